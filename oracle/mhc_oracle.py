@@ -1,0 +1,227 @@
+"""Plain float64 reference of the mHC layer, forward and backward.
+
+Test infrastructure only: see the package docstring for who may import it.
+
+Notation (openPangu 2.0 analysis notes, section 5.3):
+    h_bar  : the n-stream residual state of one token, shape [n, D]
+    x_bar  = RMSNorm(h_bar), taken over the flattened n*D row (K = n*D)
+    [r_pre, r_post, r_res] = x_bar @ W_mHC        (G = 2n + n^2 logits)
+    H_pre  = sigmoid(r_pre)         in (0, 1)     (n streams -> 1)
+    H_post = 2 * sigmoid(r_post)    in (0, 2)     (1 stream  -> n)
+    H_res  = Sinkhorn(reshape(r_res, n, n))       (n streams -> n)
+The Ascend mHC Triton operator article adds that H_res is doubly stochastic
+(non-negative, every row and column summing to 1) and that H_pre / H_post read
+n streams into one and write one stream back to n.
+
+Readings where the pages are silent (each is listed in the design doc):
+  * W_mHC is called ``phi`` here, stored [K, G] with K index k = i*D + d
+    (stream-major flattening of h_bar).
+  * Each logit group has one scalar scale alpha and every logit a bias b:
+    logits = alpha_group * (x_bar @ phi) + b, groups (pre, post, res).
+  * RMSNorm has unit weight and eps inside the square root.
+  * The res block is reshaped row-major: H_res[i, j] <- logit 2n + i*n + j.
+  * One Sinkhorn iteration = normalise rows, then normalise columns, starting
+    from exp(L); no epsilon in the denominators.
+  * x_in = sum_i H_pre[i] * x[i];  x_next[i] = sum_j H_res[i, j] * x[j]
+    + H_post[i] * y, where y is the sublayer output (an independent input).
+  * The gradient through Sinkhorn is the exact reverse-mode derivative of the
+    unrolled ``iters``-step map.
+
+All arithmetic is float64 on whatever values the caller passes (the tests pass
+the same bf16-quantised activations the GPU receives, widened to float64).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+_F = np.float64
+
+
+def _f64(a):
+    return np.asarray(a, dtype=_F)
+
+
+def group_of_logit(n: int) -> np.ndarray:
+    """Group index (0 = pre, 1 = post, 2 = res) of each of the 2n + n^2 logits.
+
+    Order [r_pre, r_post, r_res] as written in section 5.3 of the openPangu 2.0
+    notes.
+    """
+    return np.array([0] * n + [1] * n + [2] * (n * n), dtype=np.int64)
+
+
+def rmsnorm_flat(x, eps: float):
+    """RMSNorm over the flattened n*D row, unit weight (section 5.3).
+
+    x: [T, n, D].  Returns (x_bar [T, n, D], inv_rms [T]) with
+    inv_rms = 1 / sqrt(mean(x^2) + eps).
+    """
+    x = _f64(x)
+    T = x.shape[0]
+    flat = x.reshape(T, -1)
+    ms = np.mean(flat * flat, axis=1)
+    inv_rms = 1.0 / np.sqrt(ms + eps)
+    return x * inv_rms[:, None, None], inv_rms
+
+
+def project(x_bar, phi):
+    """Projection of the normalised row onto the G gate logits: x_bar @ phi.
+
+    x_bar: [T, n, D]; phi: [n*D, G] (row k = i*D + d).  Returns [T, G].
+    """
+    x_bar = _f64(x_bar)
+    T = x_bar.shape[0]
+    return x_bar.reshape(T, -1) @ _f64(phi)
+
+
+def logits_from_proj(proj, alpha, b, n: int):
+    """logits = alpha_group * proj + b, groups [pre (n), post (n), res (n^2)]."""
+    alpha = _f64(alpha)
+    scale = alpha[group_of_logit(n)]
+    return _f64(proj) * scale[None, :] + _f64(b)[None, :]
+
+
+def _sigmoid(v):
+    return 1.0 / (1.0 + np.exp(-v))
+
+
+def gates(logits, n: int):
+    """H_pre = sigmoid(r_pre), H_post = 2 sigmoid(r_post) (section 5.3)."""
+    logits = _f64(logits)
+    return _sigmoid(logits[:, :n]), 2.0 * _sigmoid(logits[:, n:2 * n])
+
+
+def sinkhorn_iterates(L, iters: int):
+    """All intermediate matrices of the Sinkhorn-Knopp map started at exp(L).
+
+    L: [T, n, n].  Returns a list [M0, P1, M1, P2, M2, ..., P_iters, M_iters]
+    where P_k = M_{k-1} with rows normalised and M_k = P_k with columns
+    normalised.  M_iters is H_res.
+    """
+    M = np.exp(_f64(L))
+    out = [M]
+    for _ in range(iters):
+        P = M / M.sum(axis=2, keepdims=True)
+        M = P / P.sum(axis=1, keepdims=True)
+        out.append(P)
+        out.append(M)
+    return out
+
+
+def sinkhorn(L, iters: int):
+    """H_res = Sinkhorn(exp(L)) after ``iters`` row-then-column rounds."""
+    return sinkhorn_iterates(L, iters)[-1]
+
+
+def sinkhorn_vjp(L, iters: int, dH):
+    """Reverse-mode derivative of ``sinkhorn`` with respect to L.
+
+    For Y = X / s with s = row sums of X:   dX = (dY - rowsum(dY * Y)) / s.
+    For Y = X / c with c = column sums:     dX = (dY - colsum(dY * Y)) / c.
+    For M0 = exp(L):                        dL = dM0 * M0.
+    """
+    its = sinkhorn_iterates(L, iters)
+    g = _f64(dH)
+    for k in range(iters, 0, -1):
+        P, M = its[2 * k - 1], its[2 * k]
+        c = P.sum(axis=1, keepdims=True)          # column sums of P
+        g = (g - np.sum(g * M, axis=1, keepdims=True)) / c
+        Mprev = its[2 * k - 2]
+        s = Mprev.sum(axis=2, keepdims=True)      # row sums of M_{k-1}
+        g = (g - np.sum(g * P, axis=2, keepdims=True)) / s
+    return g * its[0]
+
+
+def mhc_pre(x, phi, b, alpha, iters: int, eps: float):
+    """Forward of the pre side of one mHC layer for T tokens.
+
+    x: [T, n, D]; phi: [n*D, 2n+n^2]; b: [2n+n^2]; alpha: [3].
+    Returns a dict with x_in [T, D], H_pre [T, n], H_post [T, n],
+    H_res [T, n, n], proj [T, G] (x_bar @ phi), logits [T, G], inv_rms [T].
+    """
+    x = _f64(x)
+    T, n, D = x.shape
+    x_bar, inv_rms = rmsnorm_flat(x, eps)
+    proj = project(x_bar, phi)
+    logits = logits_from_proj(proj, alpha, b, n)
+    H_pre, H_post = gates(logits, n)
+    H_res = sinkhorn(logits[:, 2 * n:].reshape(T, n, n), iters)
+    x_in = np.einsum("ti,tid->td", H_pre, x)
+    return dict(x_in=x_in, H_pre=H_pre, H_post=H_post, H_res=H_res,
+                proj=proj, logits=logits, inv_rms=inv_rms)
+
+
+def mhc_post(x, y, H_post, H_res):
+    """x_next[i] = sum_j H_res[i, j] x[j] + H_post[i] y (section 5.3)."""
+    x = _f64(x)
+    return (np.einsum("tij,tjd->tid", _f64(H_res), x)
+            + _f64(H_post)[:, :, None] * _f64(y)[:, None, :])
+
+
+def mhc_post_bwd(g_next, x, y, H_post, H_res):
+    """Gradients of <g_next, mhc_post(x, y, H_post, H_res)>.
+
+    Returns dict dx [T, n, D], dy [T, D], dH_post [T, n], dH_res [T, n, n].
+    """
+    g = _f64(g_next)
+    x = _f64(x)
+    y = _f64(y)
+    dx = np.einsum("tij,tid->tjd", _f64(H_res), g)
+    dy = np.einsum("ti,tid->td", _f64(H_post), g)
+    dH_post = np.einsum("tid,td->ti", g, y)
+    dH_res = np.einsum("tid,tjd->tij", g, x)
+    return dict(dx=dx, dy=dy, dH_post=dH_post, dH_res=dH_res)
+
+
+def mhc_pre_bwd(g_in, dH_post, dH_res, x, phi, b, alpha, iters: int,
+                eps: float):
+    """Gradients of <g_in, x_in> + (terms reaching H_post, H_res).
+
+    dH_post and dH_res are the upstream gradients of the gates (as returned by
+    ``mhc_post_bwd``).  Returns dict dx [T, n, D] (the pre-side part only: the
+    H_pre mix plus the path through the projection and RMSNorm), dphi [K, G],
+    db [G], dalpha [3], and the per-token intermediates dlogits [T, G] and
+    dH_pre [T, n].
+    """
+    x = _f64(x)
+    g_in = _f64(g_in)
+    phi = _f64(phi)
+    T, n, D = x.shape
+    K = n * D
+    fwd = mhc_pre(x, phi, b, alpha, iters, eps)
+    logits, proj, inv_rms = fwd["logits"], fwd["proj"], fwd["inv_rms"]
+    H_pre = fwd["H_pre"]
+
+    # x_in = sum_i H_pre[i] x[i]
+    dH_pre = np.einsum("td,tid->ti", g_in, x)
+    dx = H_pre[:, :, None] * g_in[:, None, :]
+
+    # gates
+    s_pre = _sigmoid(logits[:, :n])
+    s_post = _sigmoid(logits[:, n:2 * n])
+    dl_pre = dH_pre * s_pre * (1.0 - s_pre)
+    dl_post = _f64(dH_post) * 2.0 * s_post * (1.0 - s_post)
+    dl_res = sinkhorn_vjp(logits[:, 2 * n:].reshape(T, n, n), iters,
+                          _f64(dH_res)).reshape(T, n * n)
+    dlogits = np.concatenate([dl_pre, dl_post, dl_res], axis=1)
+
+    # logits = alpha_group * proj + b
+    grp = group_of_logit(n)
+    db = dlogits.sum(axis=0)
+    dalpha = np.array([np.sum((dlogits * proj)[:, grp == g]) for g in range(3)])
+    dproj = dlogits * _f64(alpha)[grp][None, :]
+
+    # proj = x_bar @ phi
+    x_bar = (x * inv_rms[:, None, None]).reshape(T, K)
+    dphi = x_bar.T @ dproj
+    dx_bar = dproj @ phi.T                              # [T, K]
+
+    # x_bar = x * s, s = (mean(x^2) + eps)^(-1/2)
+    xf = x.reshape(T, K)
+    s = inv_rms[:, None]
+    dot = np.sum(dx_bar * xf, axis=1, keepdims=True)
+    dx_norm = s * dx_bar - (s ** 3) * xf * dot / K
+    dx = dx + dx_norm.reshape(T, n, D)
+    return dict(dx=dx, dphi=dphi, db=db, dalpha=dalpha, dlogits=dlogits,
+                dH_pre=dH_pre)
