@@ -1,0 +1,387 @@
+#!/usr/bin/env python
+"""Benchmark of the mHC layer on GB300: one step = mhc_pre -> mhc_post ->
+mhc_post_bwd -> mhc_pre_bwd over one batch (the whole hot path), on synthetic
+inputs resident in HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload 5] [--iters 20]
+
+Prints ONE JSON line (rank 0).  Under torchrun (N > 1) every rank runs its own
+batch of T tokens (weak scaling) and the parameter gradients dphi, db, dalpha
+are summed over ranks with one NCCL all-reduce per step, the layer's only
+exchange.  ``--impl reference`` times the float64 CPU oracle (the reference
+arm) on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "mHC fused fwd(+bwd) tokens/s and HBM GB/s vs GB300 peak at n=4, D=5120"
+UNIT = "tokens/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+STEP_OPS = ("mhc_pre", "mhc_post", "mhc_post_bwd", "mhc_pre_bwd")
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--workload", type=int, default=5)
+    p.add_argument("--iters", type=int, default=20)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    return p.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def algorithmic_bytes(w):
+    """Bytes each op must move per launch (activations once, gates, saved
+    state; phi and the parameter gradients once per launch)."""
+    a = 2 if w.dtype == "bf16" else 4
+    K, D, T, G = w.K, w.D, w.T, w.G
+    gates_pre = 4 * (w.n + w.n + w.n * w.n + G + 1)      # H_pre, H_post, H_res, proj, inv_rms
+    per_tok = {
+        "mhc_pre": a * K + a * D + gates_pre,
+        "mhc_post": a * K + a * D + 4 * (w.n + w.n * w.n) + a * K,
+        "mhc_post_bwd": 3 * a * K + 2 * a * D + 2 * 4 * (w.n + w.n * w.n),
+        "mhc_pre_bwd": a * D + 3 * a * K + 4 * (G + 1 + w.n + w.n * w.n),
+    }
+    per_launch = {"mhc_pre": 4 * K * G, "mhc_post": 0, "mhc_post_bwd": 0,
+                  "mhc_pre_bwd": 2 * 4 * K * G}
+    return {op: per_tok[op] * T + per_launch[op] for op in STEP_OPS}, per_tok
+
+
+class ClockSampler:
+    """nvidia-smi sampler for the clocks and throttle reasons of one GPU."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for r in csv.reader(io.StringIO(out)):
+            if len(r) < 9:
+                continue
+            try:
+                ts = time.mktime(time.strptime(r[0].strip().split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + r[0].strip().split(".")[1]) if "." in r[0] else 0.0
+                rows.append((ts + frac, float(r[1]), float(r[2]), r[5].strip(), r[6].strip(),
+                             r[7].strip(), r[8].strip()))
+            except (ValueError, IndexError):
+                continue
+        inside = [x for x in rows if t0 - 0.15 <= x[0] <= t1 + 0.15]
+        if len(inside) < 3:       # short timed region: nearest samples around it
+            rows.sort(key=lambda x: abs(x[0] - 0.5 * (t0 + t1)))
+            inside = rows[:5]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for x in inside:
+            for name, v in zip(names, x[3:]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(x[1] for x in inside),
+                "sm_max_mhz": max(x[2] for x in inside),
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+def oracle_rate(w, seconds: float, chunk: int = 256):
+    """Tokens/s of the float64 oracle (fwd + bwd of the whole layer) on
+    chunks of the workload, repeated for about ``seconds``."""
+    from mhc_pre_gb300 import workloads as W
+    from tests import parity as P
+    sample = W.make_inputs(w.with_(T=chunk, backward=True), device="cpu")
+    inp = {k: P.f64(v) for k, v in sample.items()}
+    done, t0 = 0, time.perf_counter()
+    while True:
+        P.run_oracle(inp, w.iters, w.eps, True)
+        done += chunk
+        if time.perf_counter() - t0 >= seconds:
+            break
+    el = time.perf_counter() - t0
+    return done / el, done, el
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from mhc_pre_gb300 import workloads as W
+    from tests import parity as P
+    w = W.WORKLOADS[args.workload].with_(iters=args.iters, backward=True)
+    # calibrate: size each step so that warmup + steps take about 2 minutes
+    rate, _, _ = oracle_rate(w, 1.0, chunk=4)
+    per_step = 120.0 / max(1, args.steps + args.warmup)
+    S = int(max(1, min(256, rate * per_step)))
+    sample = W.make_inputs(w.with_(T=S), device="cpu")
+    inp = {k: P.f64(v) for k, v in sample.items()}
+    for _ in range(args.warmup):
+        P.run_oracle(inp, w.iters, w.eps, True)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        P.run_oracle(inp, w.iters, w.eps, True)
+    el = time.perf_counter() - t0
+    value = S * args.steps / el
+    cores = len(os.sched_getaffinity(0))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, S),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"float64 NumPy oracle, fwd+bwd of the whole layer on {S} "
+                                   f"tokens per step of the {w.name} workload"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, tokens=None):
+    return {"workload": f"mhc layer fwd+bwd: {w.name}", "T": w.T if tokens is None else tokens,
+            "n": w.n, "D": w.D, "iters": w.iters, "alpha": w.alpha, "b_std": w.b_std,
+            "step": "mhc_pre+mhc_post+mhc_post_bwd+mhc_pre_bwd",
+            "l2": "inputs larger than L2 (no flush)"}
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    from mhc_pre_gb300 import binding as B
+    from mhc_pre_gb300 import build as mbuild
+    from mhc_pre_gb300 import workloads as W
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    mbuild.build()
+
+    w = W.WORKLOADS[args.workload].with_(iters=args.iters, backward=True)
+    inp = W.make_inputs(w, device=dev, seed=1000 + w.wid + 7919 * rank)
+    ws = torch.empty((max(B.pre_bwd_workspace_bytes(torch.bfloat16, w.T, w.n, w.D), 16),),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STEP_OPS) + 1)]
+          for _ in range(args.steps)]
+
+    def step(i=None):
+        e = ev[i] if i is not None else None
+        if e: e[0].record(stream)
+        f = B.mhc_pre(inp["x"], inp["phi"], inp["b"], inp["alpha"], w.iters, w.eps)
+        if e: e[1].record(stream)
+        B.mhc_post(inp["x"], inp["y"], f.H_post, f.H_res)
+        if e: e[2].record(stream)
+        pb = B.mhc_post_bwd(inp["g_next"], inp["x"], inp["y"], f.H_post, f.H_res)
+        if e: e[3].record(stream)
+        qb = B.mhc_pre_bwd(inp["g_in"], pb.dH_post, pb.dH_res, inp["x"], inp["phi"], inp["b"],
+                           inp["alpha"], f.proj, f.inv_rms, pb.dx, w.iters, workspace=ws)
+        if e: e[4].record(stream)
+        if world > 1:
+            flat = torch.cat([qb.dphi.view(-1), qb.db, qb.dalpha])
+            dist.all_reduce(flat)
+        return qb
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if B.get_last_device_error() != B.MHC_OK:
+        raise RuntimeError("device error during warm-up")
+
+    gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    sampler = ClockSampler(gpu_id) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        step(i)
+    end.record(stream)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    clocks = sampler.stop(w0, w1) if sampler else None
+    assert B.get_last_device_error() == B.MHC_OK
+
+    per_op_ms = {op: statistics.fmean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
+                 for j, op in enumerate(STEP_OPS)}
+    nbytes, per_tok = algorithmic_bytes(w)
+    peak, peak_kind = peaks()
+    kernels = {op: {"ms": per_op_ms[op], "GBps": nbytes[op] / per_op_ms[op] / 1e6,
+                    "frac_of_" + peak_kind: nbytes[op] / per_op_ms[op] / 1e6 / peak,
+                    "frac_of_8TBps_nominal": nbytes[op] / per_op_ms[op] / 1e6 / NOMINAL_HBM_GBS,
+                    "bytes": nbytes[op]}
+               for op in STEP_OPS}
+    dom = max(STEP_OPS, key=lambda op: per_op_ms[op])
+    achieved = nbytes[dom] / per_op_ms[dom] / 1e6
+    traffic = ncu_traffic(dom, w)
+
+    # ---- end to end: pinned host inputs in, parameter gradients out ----------
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, inp, step, stream, dev, world)
+
+    # ---- float64 oracle on the host cores (rank 0, N = 1) --------------------
+    cpu = None
+    if rank == 0 and world == 1:
+        rate, done, el = oracle_rate(w, args.cpu_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
+               "kind": "oracle",
+               "sample": f"float64 NumPy oracle, fwd+bwd of the whole layer, {done} tokens "
+                         f"(256-token chunks, D={w.D}) in {el:.1f} s"}
+
+    launches_per_step = launches(w)
+    value = world * w.T * args.steps / (elapsed_ms / 1e3)
+    step_bytes = sum(nbytes.values())
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic", "config": workload_config(w),
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic,
+                     "algorithmic_bytes_per_token": per_tok[dom], "tokens_per_launch": w.T},
+        "step_hbm": {"GBps": step_bytes / (elapsed_ms / args.steps) / 1e6,
+                     "frac_of_" + peak_kind: step_bytes / (elapsed_ms / args.steps) / 1e6 / peak,
+                     "frac_of_8TBps_nominal": step_bytes / (elapsed_ms / args.steps) / 1e6 / NOMINAL_HBM_GBS},
+        "kernels": kernels,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def launches(w):
+    """Kernels of this library launched per step (kernels)."""
+    from mhc_pre_gb300 import binding as B
+    return sum(B.kernel_launches(op, w.dtype, w.T, w.n, w.D) for op in STEP_OPS)
+
+
+def ncu_traffic(op, w):
+    """DRAM bytes per launch of ``op`` from the committed ncu summary, scaled
+    to this workload's token count; None when no current capture exists."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        rec = d[op]
+        return rec["bytes_per_token"] * w.T + rec.get("bytes_per_launch_fixed", 0)
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def run_e2e(args, w, inp, step, stream, dev, world):
+    import torch
+    host = {k: v.to("cpu").pin_memory() for k, v in inp.items()}
+    keys = ("x", "y", "g_in", "g_next", "phi", "b", "alpha")
+    h2d = sum(host[k].numel() * host[k].element_size() for k in keys)
+    G = w.G
+    out_h = {"dphi": torch.empty((w.K, G), pin_memory=True),
+             "db": torch.empty((G,), pin_memory=True),
+             "dalpha": torch.empty((3,), pin_memory=True)}
+    d2h = sum(v.numel() * v.element_size() for v in out_h.values())
+    steps = args.steps
+
+    def one():
+        for k in keys:
+            inp[k].copy_(host[k], non_blocking=True)
+        qb = step()
+        out_h["dphi"].copy_(qb.dphi, non_blocking=True)
+        out_h["db"].copy_(qb.db, non_blocking=True)
+        out_h["dalpha"].copy_(qb.dalpha, non_blocking=True)
+
+    for _ in range(min(3, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        one()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": world * w.T * steps / (ms / 1e3), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms / steps,
+            "path": "pinned host -> device copies, the four C-ABI calls, parameter gradients -> pinned host"}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,167 @@
+/*
+ * mhc.h -- C ABI of the GB300 (sm_103a) mHC layer library (libmhc_gb300.so).
+ *
+ * The layer is the manifold-constrained hyper-connection of the "openPangu 2.0
+ * -- architecture, training and Ascend systems" analysis notes, section 5.3:
+ * for each token t with n residual streams x[t] in R^{n x D}, K = n*D,
+ *
+ *   x_bar  = RMSNorm(x[t])                 (flattened n*D row, unit weight)
+ *   proj   = x_bar . phi                   (phi in R^{K x G}, G = 2n + n^2)
+ *   logits = alpha_group * proj + b        (groups pre | post | res)
+ *   H_pre  = sigmoid(logits[0:n])          in (0, 1)
+ *   H_post = 2 sigmoid(logits[n:2n])       in (0, 2)
+ *   H_res  = Sinkhorn(exp(reshape(logits[2n:], n, n)))   doubly stochastic
+ *   x_in   = sum_i H_pre[i] x[t, i]                          (mhc_pre)
+ *   x_next[i] = sum_j H_res[i, j] x[t, j] + H_post[i] y[t]   (mhc_post)
+ *
+ * The ranges of the gates and the doubly stochastic H_res (non-negative, rows
+ * and columns summing to 1) are those of the Ascend mHC Triton operator
+ * article (paragraph defining H^res / H^pre / H^post).  One Sinkhorn round
+ * normalises the rows, then the columns; H_res[i][j] is logit 2n + i*n + j.
+ *
+ * Conventions shared by every entry point:
+ *   - All pointers are device pointers owned by the caller.  The library
+ *     allocates no memory; scratch space is passed in (mhc_pre_bwd).
+ *   - Tensors are dense, row-major, with the shapes given per argument.
+ *     Activations (x, y, x_in, x_next, g_in, g_next, dx, dy) have type `dt`;
+ *     gates, phi, b, alpha, saved state and parameter gradients are float32.
+ *   - Every pointer must be 16-byte aligned.  n must be 4.  D must be a
+ *     multiple of 8 (bf16) or 4 (float32).  T = 0 is a no-op.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream) and
+ *     never synchronise the host.  A bad argument returns an error before
+ *     anything is launched; a failed launch returns MHC_ERR_CUDA.  Errors that
+ *     only the device can see (a bounded wait that ran out) are latched in a
+ *     device word and reported by mhc_get_last_device_error().
+ *   - Results are deterministic: no floating-point atomics.
+ */
+#ifndef MHC_GB300_H
+#define MHC_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MHC_OK = 0,
+    MHC_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad iters/eps, short workspace */
+    MHC_ERR_UNSUPPORTED = 2,  /* n != 4, D not a multiple of the vector width, iters > MHC_MAX_ITERS */
+    MHC_ERR_MISALIGNED = 3,   /* a pointer is not 16-byte aligned */
+    MHC_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
+    MHC_ERR_TIMEOUT = 5       /* a bounded device-side wait gave up (see mhc_get_last_device_error) */
+} mhc_status;
+
+typedef enum { MHC_F32 = 0, MHC_BF16 = 1 } mhc_dtype;
+
+/* Largest Sinkhorn round count the kernels accept (the backward keeps the
+ * per-round normalisers of one token in registers / local memory). */
+#define MHC_MAX_ITERS 64
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* mhc_status_string(mhc_status s);
+
+/* Library version string, e.g. "mhc_gb300 0.1.0 sm_103a". */
+const char* mhc_version(void);
+
+/* Synchronises `stream`, then reads and clears the library's device error
+ * word on the current device.  Returns MHC_OK if no kernel latched an error,
+ * MHC_ERR_TIMEOUT if a bounded wait ran out, MHC_ERR_CUDA if the
+ * synchronisation itself failed. */
+mhc_status mhc_get_last_device_error(cudaStream_t stream);
+
+/*
+ * mhc_pre -- forward of the read side (steps RMSNorm, projection, gates,
+ * Sinkhorn and the H_pre mix of section 5.3 of the openPangu 2.0 notes).
+ *
+ *   x       [T, n, D]  dt      the n-stream residual state
+ *   phi     [n*D, G]   float   projection W_mHC (row k = i*D + d)
+ *   b       [G]        float   logit bias
+ *   alpha   [3]        float   logit scales of the pre, post and res groups
+ *   iters              int     Sinkhorn rounds, 1 .. MHC_MAX_ITERS
+ *   eps                float   RMSNorm epsilon (>= 0, inside the sqrt)
+ * outputs (written):
+ *   x_in    [T, D]     dt      sum_i H_pre[i] x[i]  (fp32 sum, one rounding)
+ *   H_pre   [T, n]     float
+ *   H_post  [T, n]     float
+ *   H_res   [T, n, n]  float
+ *   proj    [T, G]     float   x_bar . phi (saved for mhc_pre_bwd)
+ *   inv_rms [T]        float   1/sqrt(mean(x^2) + eps) (saved for mhc_pre_bwd)
+ */
+mhc_status mhc_pre(mhc_dtype dt, const void* x, const float* phi,
+                   const float* b, const float* alpha, int64_t T, int n,
+                   int64_t D, int iters, float eps, void* x_in, float* H_pre,
+                   float* H_post, float* H_res, float* proj, float* inv_rms,
+                   cudaStream_t stream);
+
+/*
+ * mhc_post -- forward of the write side (residual update of section 5.3):
+ *   x_next[t, i] = sum_j H_res[t, i, j] x[t, j] + H_post[t, i] y[t]
+ *
+ *   x [T, n, D] dt; y [T, D] dt; H_post [T, n] float; H_res [T, n, n] float
+ *   x_next [T, n, D] dt (written; must not alias x or y)
+ */
+mhc_status mhc_post(mhc_dtype dt, const void* x, const void* y,
+                    const float* H_post, const float* H_res, int64_t T, int n,
+                    int64_t D, void* x_next, cudaStream_t stream);
+
+/*
+ * mhc_post_bwd -- gradients of <g_next, x_next> for mhc_post:
+ *   dx[t, j]      = sum_i H_res[t, i, j] g_next[t, i]     (written, not added)
+ *   dy[t]         = sum_i H_post[t, i] g_next[t, i]
+ *   dH_post[t, i] = <g_next[t, i], y[t]>
+ *   dH_res[t,i,j] = <g_next[t, i], x[t, j]>
+ *
+ *   g_next, x, dx [T, n, D] dt; y, dy [T, D] dt;
+ *   H_post, dH_post [T, n] float; H_res, dH_res [T, n, n] float
+ */
+mhc_status mhc_post_bwd(mhc_dtype dt, const void* g_next, const void* x,
+                        const void* y, const float* H_post, const float* H_res,
+                        int64_t T, int n, int64_t D, void* dx, void* dy,
+                        float* dH_post, float* dH_res, cudaStream_t stream);
+
+/* Number of kernels the entry point `op` ("mhc_pre", "mhc_post",
+ * "mhc_post_bwd" or "mhc_pre_bwd") launches for these sizes; -1 for an
+ * unknown op or sizes the entry point would reject.  Useful when sizing CUDA
+ * graphs or counting launches. */
+int mhc_kernel_launches(const char* op, mhc_dtype dt, int64_t T, int n, int64_t D);
+
+/* Bytes of scratch mhc_pre_bwd needs for these sizes (0 for T = 0). */
+size_t mhc_pre_bwd_workspace_bytes(mhc_dtype dt, int64_t T, int n, int64_t D);
+
+/*
+ * mhc_pre_bwd -- backward of mhc_pre given the gradient of x_in and the
+ * gradients of H_post and H_res (as produced by mhc_post_bwd).  The
+ * Sinkhorn forward is recomputed from `proj`; its derivative is the exact
+ * reverse mode of the unrolled `iters`-round map.
+ *
+ *   g_in    [T, D]     dt      dL/dx_in
+ *   dH_post [T, n]     float   dL/dH_post
+ *   dH_res  [T, n, n]  float   dL/dH_res
+ *   x, phi, b, alpha, iters        as passed to mhc_pre
+ *   proj, inv_rms      float   as written by mhc_pre
+ * outputs:
+ *   dx      [T, n, D]  dt      ACCUMULATED: dx += pre-side gradient (the
+ *                              H_pre mix plus the projection / RMSNorm path),
+ *                              so that after mhc_post_bwd it holds dL/dx
+ *   dphi    [n*D, G]   float   written
+ *   db      [G]        float   written
+ *   dalpha  [3]        float   written
+ *   workspace, ws_bytes        device scratch of at least
+ *                              mhc_pre_bwd_workspace_bytes() bytes
+ */
+mhc_status mhc_pre_bwd(mhc_dtype dt, const void* g_in, const float* dH_post,
+                       const float* dH_res, const void* x, const float* phi,
+                       const float* b, const float* alpha, const float* proj,
+                       const float* inv_rms, int64_t T, int n, int64_t D,
+                       int iters, void* dx, float* dphi, float* db,
+                       float* dalpha, void* workspace, size_t ws_bytes,
+                       cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MHC_GB300_H */

@@ -1,0 +1,362 @@
+// kernels_bwd.cu -- backward kernels of the mHC layer (sm_103a).
+//
+// post backward (one warp per token):
+//   dx[j] = sum_i H_res[i,j] g[i],  dy = sum_i H_post[i] g[i],
+//   dH_post[i] = <g[i], y>,         dH_res[i,j] = <g[i], x[j]>
+// pre backward, four launches:
+//   1. dots   (warp per token): dH_pre[i] = <g_in, x[i]>
+//   2. token  (thread per token): gate derivatives, Sinkhorn VJP from the
+//      recomputed forward, u = inv_rms * alpha_grp * dlogits and the RMSNorm
+//      coefficient of x, written to a per-token record
+//   3. main   (K slice x token block): dx += H_pre[i] g_in + phi u + coef x,
+//      and the block's partial dphi = sum_t x_t u_t^T
+//   4. reduce : dphi over token blocks, db and dalpha over tokens (fixed
+//      order, no atomics)
+// Derivation (with s = inv_rms, v = alpha_grp * dlogits, proj = s * x.phi):
+//   dx_norm = s * phi v - s^2 * x * (v . proj) / K,   dphi = sum_t s_t x_t v_t^T
+// Layer definition: "openPangu 2.0 -- architecture, training and Ascend
+// systems" notes, section 5.3; recompute instead of storing the Sinkhorn
+// iterates follows the recompute paragraph of the Ascend mHC Triton operator
+// article.
+#include "launch.h"
+#include "mhc_common.cuh"
+
+namespace mhc {
+namespace {
+
+template <typename TA>
+__global__ void __launch_bounds__(256)
+post_bwd_kernel(const TA* __restrict__ g, const TA* __restrict__ x, const TA* __restrict__ y,
+                const float* __restrict__ H_post, const float* __restrict__ H_res, int64_t T,
+                int64_t D, TA* __restrict__ dx, TA* __restrict__ dy, float* __restrict__ dH_post,
+                float* __restrict__ dH_res) {
+    constexpr int V = Vec<TA>::N;
+    const int lane = threadIdx.x & 31;
+    const int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (t >= T) return;
+    const int64_t QD = D / V;
+    const float4 hp = reinterpret_cast<const float4*>(H_post)[t];
+    const float4* hr4 = reinterpret_cast<const float4*>(H_res + t * 16);
+    const float4 r0 = hr4[0], r1 = hr4[1], r2 = hr4[2], r3 = hr4[3];
+    const float H[4][4] = {{r0.x, r0.y, r0.z, r0.w}, {r1.x, r1.y, r1.z, r1.w},
+                           {r2.x, r2.y, r2.z, r2.w}, {r3.x, r3.y, r3.z, r3.w}};
+    const float Hp[4] = {hp.x, hp.y, hp.z, hp.w};
+    float ap[4] = {0.f, 0.f, 0.f, 0.f};
+    float ar[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) ar[e] = 0.f;
+
+    const TA* gp = g + t * 4 * D;
+    const TA* xp = x + t * 4 * D;
+    const TA* yp = y + t * D;
+    for (int64_t q = lane; q < QD; q += 32) {
+        float fg[4][V], fx[4][V], fy[V];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) Vec<TA>::unpack(ld16_stream(gp + i * D + q * V), fg[i]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) Vec<TA>::unpack(ld16_stream(xp + j * D + q * V), fx[j]);
+        Vec<TA>::unpack(ld16_stream(yp + q * V), fy);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float o[V];
+#pragma unroll
+            for (int e = 0; e < V; ++e)
+                o[e] = fmaf(H[3][j], fg[3][e], fmaf(H[2][j], fg[2][e], fmaf(H[1][j], fg[1][e], H[0][j] * fg[0][e])));
+            st16_stream(dx + t * 4 * D + j * D + q * V, Vec<TA>::pack(o));
+        }
+        {
+            float o[V];
+#pragma unroll
+            for (int e = 0; e < V; ++e)
+                o[e] = fmaf(Hp[3], fg[3][e], fmaf(Hp[2], fg[2][e], fmaf(Hp[1], fg[1][e], Hp[0] * fg[0][e])));
+            st16_stream(dy + t * D + q * V, Vec<TA>::pack(o));
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int e = 0; e < V; ++e) {
+                ap[i] = fmaf(fg[i][e], fy[e], ap[i]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) ar[4 * i + j] = fmaf(fg[i][e], fx[j][e], ar[4 * i + j]);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ap[i] = warp_sum(ap[i]);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) ar[e] = warp_sum(ar[e]);
+    if (lane == 0) {
+        reinterpret_cast<float4*>(dH_post)[t] = make_float4(ap[0], ap[1], ap[2], ap[3]);
+        float4* o = reinterpret_cast<float4*>(dH_res + t * 16);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) o[v] = make_float4(ar[4 * v], ar[4 * v + 1], ar[4 * v + 2], ar[4 * v + 3]);
+    }
+}
+
+// 1. dH_pre[i] = <g_in, x[i]>, one warp per token.
+template <typename TA>
+__global__ void __launch_bounds__(256)
+pre_bwd_dots_kernel(const TA* __restrict__ g_in, const TA* __restrict__ x, int64_t T, int64_t D,
+                    float* __restrict__ rec) {
+    constexpr int V = Vec<TA>::N;
+    const int lane = threadIdx.x & 31;
+    const int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (t >= T) return;
+    const int64_t QD = D / V;
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int64_t q = lane; q < QD; q += 32) {
+        float fg[V];
+        Vec<TA>::unpack(ld16(g_in + t * D + q * V), fg);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float fx[V];
+            Vec<TA>::unpack(ld16(x + t * 4 * D + i * D + q * V), fx);
+#pragma unroll
+            for (int e = 0; e < V; ++e) a[i] = fmaf(fg[e], fx[e], a[i]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = warp_sum(a[i]);
+    if (lane == 0)
+        reinterpret_cast<float4*>(rec + t * REC + REC_DHPRE)[0] = make_float4(a[0], a[1], a[2], a[3]);
+}
+
+// 2. Per-token gate backward, one thread per token.
+__global__ void __launch_bounds__(128)
+pre_bwd_token_kernel(const float* __restrict__ dH_post, const float* __restrict__ dH_res,
+                     const float* __restrict__ b, const float* __restrict__ alpha,
+                     const float* __restrict__ proj, const float* __restrict__ inv_rms, int64_t T,
+                     int64_t K, int iters, float* __restrict__ rec) {
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (t >= T) return;
+    float* r = rec + t * REC;
+    float pj[NG];
+#pragma unroll
+    for (int v = 0; v < NG / 4; ++v) {
+        const float4 p = reinterpret_cast<const float4*>(proj + t * NG)[v];
+        pj[4 * v] = p.x; pj[4 * v + 1] = p.y; pj[4 * v + 2] = p.z; pj[4 * v + 3] = p.w;
+    }
+    float lg[NG];
+    make_logits(pj, alpha, b, lg);
+    const float4 dhp4 = reinterpret_cast<const float4*>(r + REC_DHPRE)[0];
+    const float4 dhq4 = reinterpret_cast<const float4*>(dH_post)[t];
+    const float dhp[4] = {dhp4.x, dhp4.y, dhp4.z, dhp4.w};
+    const float dhq[4] = {dhq4.x, dhq4.y, dhq4.z, dhq4.w};
+    float dl[NG], hpre[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float sp = sigmoid_f(lg[i]);
+        const float sq = sigmoid_f(lg[NS + i]);
+        hpre[i] = sp;
+        dl[i] = dhp[i] * sp * (1.0f - sp);
+        dl[NS + i] = dhq[i] * 2.0f * sq * (1.0f - sq);
+    }
+    float dhr[16];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        const float4 d = reinterpret_cast<const float4*>(dH_res + t * 16)[v];
+        dhr[4 * v] = d.x; dhr[4 * v + 1] = d.y; dhr[4 * v + 2] = d.z; dhr[4 * v + 3] = d.w;
+    }
+    sinkhorn_vjp(lg + 2 * NS, iters, dhr, dl + 2 * NS);
+
+    const float s = inv_rms[t];
+    const float a[3] = {alpha[0], alpha[1], alpha[2]};
+    float vp = 0.f, da[3] = {0.f, 0.f, 0.f};
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+        const int grp = group_of(g);
+        const float v = a[grp] * dl[g];
+        vp = fmaf(v, pj[g], vp);
+        da[grp] = fmaf(dl[g], pj[g], da[grp]);
+        r[REC_U + g] = s * v;
+        r[REC_DL + g] = dl[g];
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r[REC_HPRE + i] = hpre[i];
+    r[REC_COEF] = -s * s * vp / static_cast<float>(K);
+#pragma unroll
+    for (int c = 0; c < 3; ++c) r[REC_DA + c] = da[c];
+}
+
+// 3. dx += H_pre[i] g_in + phi u + coef x over a K slice, and the partial
+//    dphi of a token block.  Each thread owns two consecutive k.
+constexpr int MB_THREADS = 128;
+constexpr int MB_KS = 2 * MB_THREADS;   // K elements per CTA
+constexpr int MB_TCH = 32;              // tokens staged per chunk
+
+template <typename TA> struct Pair;
+template <> struct Pair<__nv_bfloat16> {
+    __device__ __forceinline__ static float2 load(const __nv_bfloat16* p) {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    }
+    __device__ __forceinline__ static void store(__nv_bfloat16* p, float2 v) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
+        *reinterpret_cast<__nv_bfloat162*>(p) = h;
+    }
+};
+template <> struct Pair<float> {
+    __device__ __forceinline__ static float2 load(const float* p) { return *reinterpret_cast<const float2*>(p); }
+    __device__ __forceinline__ static void store(float* p, float2 v) { *reinterpret_cast<float2*>(p) = v; }
+};
+
+template <typename TA>
+__global__ void __launch_bounds__(MB_THREADS)
+pre_bwd_main_kernel(const TA* __restrict__ g_in, const TA* __restrict__ x,
+                    const float* __restrict__ phi, const float* __restrict__ rec, int64_t T,
+                    int64_t D, int64_t tb, TA* __restrict__ dx, float* __restrict__ part) {
+    __shared__ __align__(16) float rs[MB_TCH][32];   // u[24], H_pre[4], coef, pad
+    const int64_t K = 4 * D;
+    const int64_t k0 = static_cast<int64_t>(blockIdx.x) * MB_KS + 2 * threadIdx.x;
+    const bool active = k0 < K;
+    const int si = active ? static_cast<int>(k0 / D) : 0;
+    const int64_t d0 = active ? k0 - si * D : 0;
+    const int64_t tbeg = static_cast<int64_t>(blockIdx.y) * tb;
+    const int64_t tend = tbeg + tb < T ? tbeg + tb : T;
+
+    float ph0[NG], ph1[NG], acc0[NG], acc1[NG];
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+        ph0[g] = active ? phi[k0 * NG + g] : 0.f;
+        ph1[g] = active ? phi[(k0 + 1) * NG + g] : 0.f;
+        acc0[g] = acc1[g] = 0.f;
+    }
+    for (int64_t c0 = tbeg; c0 < tend; c0 += MB_TCH) {
+        const int nt = static_cast<int>(tend - c0 < MB_TCH ? tend - c0 : MB_TCH);
+        __syncthreads();
+        for (int q = threadIdx.x; q < MB_TCH * 8; q += MB_THREADS) {
+            const int tt = q >> 3, v = q & 7;
+            float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (tt < nt) val = reinterpret_cast<const float4*>(rec + (c0 + tt) * REC)[v];
+            reinterpret_cast<float4*>(&rs[tt][0])[v] = val;
+        }
+        __syncthreads();
+        if (!active) continue;
+        for (int tt = 0; tt < nt; ++tt) {
+            const int64_t t = c0 + tt;
+            const float2 xv = Pair<TA>::load(x + t * K + k0);
+            const float2 gv = Pair<TA>::load(g_in + t * D + d0);
+            const float2 dv = Pair<TA>::load(dx + t * K + k0);
+            const float* u = rs[tt];
+            const float hpre = u[REC_HPRE + si], coef = u[REC_COEF];
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int g = 0; g < NG; ++g) {
+                s0 = fmaf(ph0[g], u[g], s0);
+                s1 = fmaf(ph1[g], u[g], s1);
+                acc0[g] = fmaf(xv.x, u[g], acc0[g]);
+                acc1[g] = fmaf(xv.y, u[g], acc1[g]);
+            }
+            float2 o;
+            o.x = dv.x + fmaf(hpre, gv.x, fmaf(coef, xv.x, s0));
+            o.y = dv.y + fmaf(hpre, gv.y, fmaf(coef, xv.y, s1));
+            Pair<TA>::store(dx + t * K + k0, o);
+        }
+    }
+    if (active) {
+        float* p = part + (static_cast<int64_t>(blockIdx.y) * K + k0) * NG;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) { p[g] = acc0[g]; p[NG + g] = acc1[g]; }
+    }
+}
+
+// 4a. dphi = sum over token blocks of the partials (fixed order).
+__global__ void __launch_bounds__(256)
+pre_bwd_reduce_phi_kernel(const float* __restrict__ part, int64_t nb, int64_t n4,
+                          float* __restrict__ dphi) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        float4 s = reinterpret_cast<const float4*>(part)[i];
+        for (int64_t bb = 1; bb < nb; ++bb) {
+            const float4 v = reinterpret_cast<const float4*>(part)[bb * n4 + i];
+            s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+        }
+        reinterpret_cast<float4*>(dphi)[i] = s;
+    }
+}
+
+// 4b. db[g] = sum_t dlogits[t, g]; dalpha[c] = sum_t da[t, c].  One warp per
+//     output column, fixed summation order.
+__global__ void __launch_bounds__(1024)
+pre_bwd_reduce_bias_kernel(const float* __restrict__ rec, int64_t T, float* __restrict__ db,
+                           float* __restrict__ dalpha) {
+    const int lane = threadIdx.x & 31, col = threadIdx.x >> 5;
+    if (col >= NG + 3) return;
+    const int off = col < NG ? REC_DL + col : REC_DA + (col - NG);
+    float s = 0.f;
+    for (int64_t t = lane; t < T; t += 32) s += rec[t * REC + off];
+    s = warp_sum(s);
+    if (lane == 0) {
+        if (col < NG) db[col] = s;
+        else dalpha[col - NG] = s;
+    }
+}
+
+}  // namespace
+
+PreBwdPlan pre_bwd_plan(int64_t T, int64_t D) {
+    PreBwdPlan p{};
+    const int64_t K = 4 * D;
+    int64_t nb = (T + 255) / 256;
+    if (nb > 16) nb = 16;
+    if (nb < 1) nb = 1;
+    p.nb = nb;
+    p.tb = (T + nb - 1) / nb;
+    p.rec_bytes = static_cast<size_t>(T) * REC * sizeof(float);
+    p.part_bytes = static_cast<size_t>(nb) * K * NG * sizeof(float);
+    p.total_bytes = T > 0 ? p.rec_bytes + p.part_bytes : 0;
+    return p;
+}
+
+cudaError_t launch_post_bwd(bool bf16, const void* g, const void* x, const void* y,
+                            const float* H_post, const float* H_res, int64_t T, int64_t D,
+                            void* dx, void* dy, float* dH_post, float* dH_res, cudaStream_t s) {
+    const dim3 grid(static_cast<unsigned>((T * 32 + 255) / 256));
+    if (bf16)
+        post_bwd_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+            static_cast<const __nv_bfloat16*>(g), static_cast<const __nv_bfloat16*>(x),
+            static_cast<const __nv_bfloat16*>(y), H_post, H_res, T, D, static_cast<__nv_bfloat16*>(dx),
+            static_cast<__nv_bfloat16*>(dy), dH_post, dH_res);
+    else
+        post_bwd_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(g), static_cast<const float*>(x),
+                                                    static_cast<const float*>(y), H_post, H_res, T, D,
+                                                    static_cast<float*>(dx), static_cast<float*>(dy),
+                                                    dH_post, dH_res);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pre_bwd(bool bf16, const void* g_in, const float* dH_post,
+                           const float* dH_res, const void* x, const float* phi, const float* b,
+                           const float* alpha, const float* proj, const float* inv_rms, int64_t T,
+                           int64_t D, int iters, void* dx, float* dphi, float* db, float* dalpha,
+                           void* ws, cudaStream_t s) {
+    const PreBwdPlan p = pre_bwd_plan(T, D);
+    const int64_t K = 4 * D;
+    float* rec = static_cast<float*>(ws);
+    float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + p.rec_bytes);
+    const dim3 gw(static_cast<unsigned>((T * 32 + 255) / 256));
+    const dim3 gt(static_cast<unsigned>((T + 127) / 128));
+    const dim3 gm(static_cast<unsigned>((K + MB_KS - 1) / MB_KS), static_cast<unsigned>(p.nb));
+    if (bf16) {
+        pre_bwd_dots_kernel<__nv_bfloat16><<<gw, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(g_in),
+                                                              static_cast<const __nv_bfloat16*>(x), T, D, rec);
+        pre_bwd_token_kernel<<<gt, 128, 0, s>>>(dH_post, dH_res, b, alpha, proj, inv_rms, T, K, iters, rec);
+        pre_bwd_main_kernel<__nv_bfloat16><<<gm, MB_THREADS, 0, s>>>(
+            static_cast<const __nv_bfloat16*>(g_in), static_cast<const __nv_bfloat16*>(x), phi, rec, T, D,
+            p.tb, static_cast<__nv_bfloat16*>(dx), part);
+    } else {
+        pre_bwd_dots_kernel<float><<<gw, 256, 0, s>>>(static_cast<const float*>(g_in),
+                                                      static_cast<const float*>(x), T, D, rec);
+        pre_bwd_token_kernel<<<gt, 128, 0, s>>>(dH_post, dH_res, b, alpha, proj, inv_rms, T, K, iters, rec);
+        pre_bwd_main_kernel<float><<<gm, MB_THREADS, 0, s>>>(static_cast<const float*>(g_in),
+                                                             static_cast<const float*>(x), phi, rec, T, D,
+                                                             p.tb, static_cast<float*>(dx), part);
+    }
+    const int64_t n4 = K * NG / 4;
+    const dim3 gr(static_cast<unsigned>((n4 + 255) / 256 < 4096 ? (n4 + 255) / 256 : 4096));
+    pre_bwd_reduce_phi_kernel<<<gr, 256, 0, s>>>(part, p.nb, n4, dphi);
+    pre_bwd_reduce_bias_kernel<<<1, 1024, 0, s>>>(rec, T, db, dalpha);
+    return cudaGetLastError();
+}
+
+}  // namespace mhc

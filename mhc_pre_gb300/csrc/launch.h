@@ -1,0 +1,52 @@
+// launch.h -- host-side launchers shared between the ABI layer and the kernel
+// translation units (internal to libmhc_gb300.so, C++ linkage).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mhc {
+
+// Record per token written by the pre backward's per-token kernel (floats).
+constexpr int REC = 64;
+constexpr int REC_U = 0;        // [0, 24)  u = inv_rms * alpha_grp * dlogits
+constexpr int REC_HPRE = 24;    // [24, 28) H_pre
+constexpr int REC_COEF = 28;    // 28       coefficient of x in the RMSNorm backward
+constexpr int REC_DL = 32;      // [32, 56) dlogits
+constexpr int REC_DA = 56;      // [56, 59) per-token dalpha terms
+constexpr int REC_DHPRE = 60;   // [60, 64) dH_pre
+
+// Sizes of the pre backward's dphi partial reduction.
+struct PreBwdPlan {
+    int64_t nb;          // token blocks (dphi partials)
+    int64_t tb;          // tokens per block
+    size_t rec_bytes;    // T * REC floats
+    size_t part_bytes;   // nb * K * NG floats
+    size_t total_bytes;
+};
+PreBwdPlan pre_bwd_plan(int64_t T, int64_t D);
+
+// Forward (CUDA-core path: projection + gates, then the H_pre mix).
+cudaError_t launch_pre_cc(bool bf16, const void* x, const float* phi, const float* b,
+                          const float* alpha, int64_t T, int64_t D, int iters, float eps,
+                          void* x_in, float* H_pre, float* H_post, float* H_res,
+                          float* proj, float* inv_rms, cudaStream_t s);
+
+cudaError_t launch_post(bool bf16, const void* x, const void* y, const float* H_post,
+                        const float* H_res, int64_t T, int64_t D, void* x_next,
+                        cudaStream_t s);
+
+cudaError_t launch_post_bwd(bool bf16, const void* g, const void* x, const void* y,
+                            const float* H_post, const float* H_res, int64_t T, int64_t D,
+                            void* dx, void* dy, float* dH_post, float* dH_res,
+                            cudaStream_t s);
+
+cudaError_t launch_pre_bwd(bool bf16, const void* g_in, const float* dH_post,
+                           const float* dH_res, const void* x, const float* phi,
+                           const float* b, const float* alpha, const float* proj,
+                           const float* inv_rms, int64_t T, int64_t D, int iters, void* dx,
+                           float* dphi, float* db, float* dalpha, void* ws,
+                           cudaStream_t s);
+
+}  // namespace mhc

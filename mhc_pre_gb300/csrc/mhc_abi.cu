@@ -1,0 +1,150 @@
+// mhc_abi.cu -- the extern "C" entry points of libmhc_gb300.so.
+//
+// Host-side validation and dispatch only: every step of the layer runs in the
+// kernels of kernels_fwd.cu, kernels_bwd.cu and pre_tc.cu.  Nothing here
+// allocates memory or synchronises the host (mhc_get_last_device_error
+// synchronises the given stream by contract).
+#include <math.h>
+#include <string.h>
+
+#include "../../include/mhc.h"
+#include "launch.h"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks shared by every entry point.  `ptrs` must all be non-null and
+// 16-byte aligned when T > 0.
+mhc_status check_common(mhc_dtype dt, int64_t T, int n, int64_t D, const void* const* ptrs,
+                        int nptr) {
+    if (dt != MHC_F32 && dt != MHC_BF16) return MHC_ERR_INVALID_ARG;
+    if (T < 0 || D <= 0) return MHC_ERR_INVALID_ARG;
+    if (n != 4) return MHC_ERR_UNSUPPORTED;
+    const int64_t vec = dt == MHC_BF16 ? 8 : 4;
+    if (D % vec != 0) return MHC_ERR_UNSUPPORTED;
+    // keep every element index of x (T * n * D) far inside int64 and the
+    // grid dimensions inside their limits
+    if (T > (int64_t(1) << 31) || D > (int64_t(1) << 24)) return MHC_ERR_UNSUPPORTED;
+    if (T == 0) return MHC_OK;
+    for (int i = 0; i < nptr; ++i) {
+        if (ptrs[i] == nullptr) return MHC_ERR_INVALID_ARG;
+        if (!aligned16(ptrs[i])) return MHC_ERR_MISALIGNED;
+    }
+    return MHC_OK;
+}
+
+mhc_status check_iters(int iters) {
+    if (iters < 1) return MHC_ERR_INVALID_ARG;
+    if (iters > MHC_MAX_ITERS) return MHC_ERR_UNSUPPORTED;
+    return MHC_OK;
+}
+
+mhc_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA; }
+
+}  // namespace
+
+namespace mhc {
+// Defined in pre_tc.cu: the tensor-core pre forward (bf16).  Returns
+// cudaErrorNotSupported when the shape is outside what it covers.
+cudaError_t launch_pre_tc(const void* x, const float* phi, const float* b, const float* alpha,
+                          int64_t T, int64_t D, int iters, float eps, void* x_in, float* H_pre,
+                          float* H_post, float* H_res, float* proj, float* inv_rms,
+                          cudaStream_t s);
+bool pre_tc_supports(int64_t T, int64_t D);
+cudaError_t read_and_clear_device_error(unsigned* word, cudaStream_t s);
+}  // namespace mhc
+
+extern "C" {
+
+const char* mhc_status_string(mhc_status s) {
+    switch (s) {
+        case MHC_OK: return "MHC_OK";
+        case MHC_ERR_INVALID_ARG: return "MHC_ERR_INVALID_ARG: null pointer, bad size, iters, eps or workspace";
+        case MHC_ERR_UNSUPPORTED: return "MHC_ERR_UNSUPPORTED: n != 4, D not a multiple of the vector width, or iters too large";
+        case MHC_ERR_MISALIGNED: return "MHC_ERR_MISALIGNED: a pointer is not 16-byte aligned";
+        case MHC_ERR_CUDA: return "MHC_ERR_CUDA: a CUDA call or kernel launch failed";
+        case MHC_ERR_TIMEOUT: return "MHC_ERR_TIMEOUT: a bounded device-side wait gave up";
+    }
+    return "MHC_ERR_UNKNOWN";
+}
+
+const char* mhc_version(void) { return "mhc_gb300 0.1.0 sm_103a"; }
+
+mhc_status mhc_get_last_device_error(cudaStream_t stream) {
+    unsigned word = 0;
+    if (mhc::read_and_clear_device_error(&word, stream) != cudaSuccess) return MHC_ERR_CUDA;
+    return word == 0 ? MHC_OK : MHC_ERR_TIMEOUT;
+}
+
+mhc_status mhc_pre(mhc_dtype dt, const void* x, const float* phi, const float* b,
+                   const float* alpha, int64_t T, int n, int64_t D, int iters, float eps,
+                   void* x_in, float* H_pre, float* H_post, float* H_res, float* proj,
+                   float* inv_rms, cudaStream_t stream) {
+    const void* ptrs[] = {x, phi, b, alpha, x_in, H_pre, H_post, H_res, proj, inv_rms};
+    mhc_status st = check_common(dt, T, n, D, ptrs, 10);
+    if (st != MHC_OK) return st;
+    if ((st = check_iters(iters)) != MHC_OK) return st;
+    if (!(eps >= 0.0f) || !isfinite(eps)) return MHC_ERR_INVALID_ARG;
+    if (T == 0) return MHC_OK;
+    if (dt == MHC_BF16 && mhc::pre_tc_supports(T, D))
+        return from_cuda(mhc::launch_pre_tc(x, phi, b, alpha, T, D, iters, eps, x_in, H_pre, H_post,
+                                            H_res, proj, inv_rms, stream));
+    return from_cuda(mhc::launch_pre_cc(dt == MHC_BF16, x, phi, b, alpha, T, D, iters, eps, x_in,
+                                        H_pre, H_post, H_res, proj, inv_rms, stream));
+}
+
+mhc_status mhc_post(mhc_dtype dt, const void* x, const void* y, const float* H_post,
+                    const float* H_res, int64_t T, int n, int64_t D, void* x_next,
+                    cudaStream_t stream) {
+    const void* ptrs[] = {x, y, H_post, H_res, x_next};
+    mhc_status st = check_common(dt, T, n, D, ptrs, 5);
+    if (st != MHC_OK || T == 0) return st;
+    return from_cuda(mhc::launch_post(dt == MHC_BF16, x, y, H_post, H_res, T, D, x_next, stream));
+}
+
+mhc_status mhc_post_bwd(mhc_dtype dt, const void* g_next, const void* x, const void* y,
+                        const float* H_post, const float* H_res, int64_t T, int n, int64_t D,
+                        void* dx, void* dy, float* dH_post, float* dH_res, cudaStream_t stream) {
+    const void* ptrs[] = {g_next, x, y, H_post, H_res, dx, dy, dH_post, dH_res};
+    mhc_status st = check_common(dt, T, n, D, ptrs, 9);
+    if (st != MHC_OK || T == 0) return st;
+    return from_cuda(mhc::launch_post_bwd(dt == MHC_BF16, g_next, x, y, H_post, H_res, T, D, dx, dy,
+                                          dH_post, dH_res, stream));
+}
+
+int mhc_kernel_launches(const char* op, mhc_dtype dt, int64_t T, int n, int64_t D) {
+    if (op == nullptr) return -1;
+    const void* none[] = {nullptr};
+    if (check_common(dt, T, n, D, none, 0) != MHC_OK) return -1;
+    if (T == 0) return 0;
+    if (strcmp(op, "mhc_pre") == 0) return dt == MHC_BF16 && mhc::pre_tc_supports(T, D) ? 1 : 2;
+    if (strcmp(op, "mhc_post") == 0 || strcmp(op, "mhc_post_bwd") == 0) return 1;
+    if (strcmp(op, "mhc_pre_bwd") == 0) return 5;
+    return -1;
+}
+
+size_t mhc_pre_bwd_workspace_bytes(mhc_dtype dt, int64_t T, int n, int64_t D) {
+    (void)dt;
+    if (T <= 0 || n != 4 || D <= 0) return 0;
+    return mhc::pre_bwd_plan(T, D).total_bytes;
+}
+
+mhc_status mhc_pre_bwd(mhc_dtype dt, const void* g_in, const float* dH_post, const float* dH_res,
+                       const void* x, const float* phi, const float* b, const float* alpha,
+                       const float* proj, const float* inv_rms, int64_t T, int n, int64_t D,
+                       int iters, void* dx, float* dphi, float* db, float* dalpha,
+                       void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    const void* ptrs[] = {g_in, dH_post, dH_res, x, phi, b, alpha, proj, inv_rms,
+                          dx, dphi, db, dalpha, workspace};
+    mhc_status st = check_common(dt, T, n, D, ptrs, 14);
+    if (st != MHC_OK) return st;
+    if ((st = check_iters(iters)) != MHC_OK) return st;
+    if (T == 0) return MHC_OK;
+    if (ws_bytes < mhc::pre_bwd_plan(T, D).total_bytes) return MHC_ERR_INVALID_ARG;
+    return from_cuda(mhc::launch_pre_bwd(dt == MHC_BF16, g_in, dH_post, dH_res, x, phi, b, alpha,
+                                         proj, inv_rms, T, D, iters, dx, dphi, db, dalpha,
+                                         workspace, stream));
+}
+
+}  // extern "C"
