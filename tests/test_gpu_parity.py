@@ -33,7 +33,7 @@ def _check(w, iters=None, backward=None, keys=None):
     dev = _dev()
     iters = w.iters if iters is None else iters
     backward = w.backward if backward is None else backward
-    gi, ci = _inputs(w, dev)
+    gi, ci = _inputs(w.with_(backward=backward), dev)
     got = P.run_gpu(gi, iters, w.eps, backward)
     ref = P.run_oracle(ci, iters, w.eps, backward)
     P.compare(got, ref, fp32=(w.dtype == "f32"), keys=keys)
