@@ -84,7 +84,15 @@ __device__ __forceinline__ float warp_sum(float v) {
 // ------------------------------------------------------------------------
 __device__ __forceinline__ int group_of(int g) { return g < NS ? 0 : (g < 2 * NS ? 1 : 2); }
 
-__device__ __forceinline__ float sigmoid_f(float v) { return 1.0f / (1.0f + expf(-v)); }
+// Hardware reciprocal approximation (rcp.approx.f32, within about one ulp);
+// the Sinkhorn normalisers and gates tolerate it by orders of magnitude.
+__device__ __forceinline__ float fast_rcp(float v) {
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+__device__ __forceinline__ float sigmoid_f(float v) { return fast_rcp(1.0f + expf(-v)); }
 
 // logits[g] = alpha[group(g)] * proj[g] + b[g]  (one fused multiply-add, so
 // the backward reproduces the forward's logits bit for bit).
@@ -113,7 +121,7 @@ __device__ __forceinline__ void normalise_rows(float (&M)[16], float* sums) {
     for (int i = 0; i < 4; ++i) {
         const float s = (M[4 * i] + M[4 * i + 1]) + (M[4 * i + 2] + M[4 * i + 3]);
         if (sums) sums[i] = s;
-        const float r = __frcp_rn(s);
+        const float r = fast_rcp(s);
 #pragma unroll
         for (int j = 0; j < 4; ++j) M[4 * i + j] *= r;
     }
@@ -124,7 +132,7 @@ __device__ __forceinline__ void normalise_cols(float (&M)[16], float* sums) {
     for (int j = 0; j < 4; ++j) {
         const float c = (M[j] + M[4 + j]) + (M[8 + j] + M[12 + j]);
         if (sums) sums[j] = c;
-        const float r = __frcp_rn(c);
+        const float r = fast_rcp(c);
 #pragma unroll
         for (int i = 0; i < 4; ++i) M[4 * i + j] *= r;
     }
