@@ -160,6 +160,41 @@ mhc_status mhc_pre_bwd(mhc_dtype dt, const void* g_in, const float* dH_post,
                        float* dalpha, void* workspace, size_t ws_bytes,
                        cudaStream_t stream);
 
+/* Size of the fixed device scratch array behind mhc_pre_bwd_noalloc. */
+#define MHC_PRE_BWD_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * mhc_pre_bwd_noalloc -- mhc_pre_bwd for callers that cannot allocate device
+ * memory.  (The pages have no counterpart: this is a packaging variant.)
+ *
+ * mhc_pre_bwd needs caller-provided scratch.  Some callers cannot provide
+ * it: a custom-op or plugin interface that hands an op its tensors but no
+ * workspace, a runtime that plans every device allocation up front and
+ * forbids allocating once it runs, or a latency-bound loop that cannot afford
+ * cudaMalloc's implicit device synchronisation.  This entry point takes its
+ * scratch from a fixed array inside the library's device memory instead and
+ * calls no allocating routine.
+ *
+ * Arguments and results are those of mhc_pre_bwd without the workspace.
+ * Limits and behaviour:
+ *   - The array holds MHC_PRE_BWD_NOALLOC_SCRATCH_BYTES (16 MiB) on every GPU
+ *     that loads the library, until the process exits.  The call returns
+ *     MHC_ERR_UNSUPPORTED when T * 256 bytes of per-token records plus one
+ *     4*D x 24 float32 partial of dphi exceed it (for D = 5120: T <= 57,856).
+ *   - The first call on a device looks up the array's device address on that
+ *     device (cudaGetSymbolAddress); make that first call before any stream
+ *     capture.
+ *   - All calls share the array; calls that overlap on the GPU race on it.
+ *     Every element is written before it is read, so no state carries over
+ *     from one call to the next.
+ */
+mhc_status mhc_pre_bwd_noalloc(mhc_dtype dt, const void* g_in, const float* dH_post,
+                               const float* dH_res, const void* x, const float* phi,
+                               const float* b, const float* alpha, const float* proj,
+                               const float* inv_rms, int64_t T, int n, int64_t D, int iters,
+                               void* dx, float* dphi, float* db, float* dalpha,
+                               cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -26,7 +26,7 @@ MAX_ITERS = 64
 
 EXPORTS = ("mhc_status_string", "mhc_version", "mhc_get_last_device_error",
            "mhc_pre", "mhc_post", "mhc_post_bwd", "mhc_kernel_launches",
-           "mhc_pre_bwd_workspace_bytes", "mhc_pre_bwd")
+           "mhc_pre_bwd_workspace_bytes", "mhc_pre_bwd", "mhc_pre_bwd_noalloc")
 
 PreOut = namedtuple("PreOut", "x_in H_pre H_post H_res proj inv_rms")
 PostBwdOut = namedtuple("PostBwdOut", "dx dy dH_post dH_res")
@@ -46,6 +46,8 @@ _SIGS = {
     "mhc_pre_bwd_workspace_bytes": ([_I, _I64, _I, _I64], ctypes.c_size_t),
     "mhc_pre_bwd": ([_I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I, _I64,
                      _I, _P, _P, _P, _P, _P, ctypes.c_size_t, _P], _I),
+    "mhc_pre_bwd_noalloc": ([_I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I,
+                             _I64, _I, _P, _P, _P, _P, _P], _I),
 }
 
 _lib = None
@@ -194,6 +196,29 @@ def mhc_pre_bwd(g_in, dH_post, dH_res, x, phi, b, alpha, proj, inv_rms, dx,
                            _ptr(workspace), workspace.numel() * workspace.element_size(),
                            _stream(x.device))
     _check(st, "mhc_pre_bwd")
+    return PreBwdOut(dx, dphi, db, dalpha)
+
+
+def mhc_pre_bwd_noalloc(g_in, dH_post, dH_res, x, phi, b, alpha, proj, inv_rms,
+                        dx, iters: int = 20):
+    """mhc_pre_bwd with the library's fixed scratch array instead of a
+    caller workspace (for callers that cannot allocate device memory).
+    ``dx`` is accumulated in place; the outputs dphi, db, dalpha are allocated
+    here by torch only because this binding returns new tensors."""
+    T, n, D = x.shape
+    G = 2 * n + n * n
+    if not (g_in.dtype == x.dtype == dx.dtype):
+        raise TypeError("g_in, x and dx must share a dtype")
+    f32 = dict(dtype=torch.float32, device=x.device)
+    dphi = torch.empty((n * D, G), **f32)
+    db = torch.empty((G,), **f32)
+    dalpha = torch.empty((3,), **f32)
+    st = lib().mhc_pre_bwd_noalloc(
+        _dtype_code(x), _ptr(g_in), _ptr(_f32(dH_post, "dH_post")), _ptr(_f32(dH_res, "dH_res")),
+        _ptr(x), _ptr(_f32(phi, "phi")), _ptr(_f32(b, "b")), _ptr(_f32(alpha, "alpha")),
+        _ptr(_f32(proj, "proj")), _ptr(_f32(inv_rms, "inv_rms")), T, n, D, iters, _ptr(dx),
+        _ptr(dphi), _ptr(db), _ptr(dalpha), _stream(x.device))
+    _check(st, "mhc_pre_bwd_noalloc")
     return PreBwdOut(dx, dphi, db, dalpha)
 
 

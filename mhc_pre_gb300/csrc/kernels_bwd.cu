@@ -359,4 +359,42 @@ cudaError_t launch_pre_bwd(bool bf16, const void* g_in, const float* dH_post,
     return cudaGetLastError();
 }
 
+// The same launch sequence with the number of dphi token blocks chosen by
+// the caller (scratch = T * REC floats of records, then nb * K * NG floats of
+// partials); used by the entry point whose scratch has a fixed size.
+cudaError_t launch_pre_bwd_blocks(bool bf16, const void* g_in, const float* dH_post,
+                                  const float* dH_res, const void* x, const float* phi,
+                                  const float* b, const float* alpha, const float* proj,
+                                  const float* inv_rms, int64_t T, int64_t D, int iters, void* dx,
+                                  float* dphi, float* db, float* dalpha, void* ws, int64_t nb,
+                                  cudaStream_t s) {
+    const int64_t K = 4 * D;
+    const int64_t tb = (T + nb - 1) / nb;
+    float* rec = static_cast<float*>(ws);
+    float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + static_cast<size_t>(T) * REC * sizeof(float));
+    const dim3 gw(static_cast<unsigned>((T * 32 + 255) / 256));
+    const dim3 gt(static_cast<unsigned>((T + 127) / 128));
+    const dim3 gm(static_cast<unsigned>((K + MB_KS - 1) / MB_KS), static_cast<unsigned>(nb));
+    if (bf16) {
+        pre_bwd_dots_kernel<__nv_bfloat16><<<gw, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(g_in),
+                                                              static_cast<const __nv_bfloat16*>(x), T, D, rec);
+        pre_bwd_token_kernel<<<gt, 128, 0, s>>>(dH_post, dH_res, b, alpha, proj, inv_rms, T, K, iters, rec);
+        pre_bwd_main_kernel<__nv_bfloat16><<<gm, MB_THREADS, 0, s>>>(
+            static_cast<const __nv_bfloat16*>(g_in), static_cast<const __nv_bfloat16*>(x), phi, rec, T, D,
+            tb, static_cast<__nv_bfloat16*>(dx), part);
+    } else {
+        pre_bwd_dots_kernel<float><<<gw, 256, 0, s>>>(static_cast<const float*>(g_in),
+                                                      static_cast<const float*>(x), T, D, rec);
+        pre_bwd_token_kernel<<<gt, 128, 0, s>>>(dH_post, dH_res, b, alpha, proj, inv_rms, T, K, iters, rec);
+        pre_bwd_main_kernel<float><<<gm, MB_THREADS, 0, s>>>(static_cast<const float*>(g_in),
+                                                             static_cast<const float*>(x), phi, rec, T, D,
+                                                             tb, static_cast<float*>(dx), part);
+    }
+    const int64_t n4 = K * NG / 4;
+    const dim3 gr(static_cast<unsigned>((n4 + 255) / 256 < 4096 ? (n4 + 255) / 256 : 4096));
+    pre_bwd_reduce_phi_kernel<<<gr, 256, 0, s>>>(part, nb, n4, dphi);
+    pre_bwd_reduce_bias_kernel<<<1, 1024, 0, s>>>(rec, T, db, dalpha);
+    return cudaGetLastError();
+}
+
 }  // namespace mhc

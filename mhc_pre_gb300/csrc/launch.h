@@ -49,4 +49,11 @@ cudaError_t launch_pre_bwd(bool bf16, const void* g_in, const float* dH_post,
                            float* dphi, float* db, float* dalpha, void* ws,
                            cudaStream_t s);
 
+cudaError_t launch_pre_bwd_blocks(bool bf16, const void* g_in, const float* dH_post,
+                                  const float* dH_res, const void* x, const float* phi,
+                                  const float* b, const float* alpha, const float* proj,
+                                  const float* inv_rms, int64_t T, int64_t D, int iters, void* dx,
+                                  float* dphi, float* db, float* dalpha, void* ws, int64_t nb,
+                                  cudaStream_t s);
+
 }  // namespace mhc

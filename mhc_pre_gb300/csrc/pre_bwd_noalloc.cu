@@ -1,0 +1,91 @@
+// pre_bwd_noalloc.cu -- mhc_pre_bwd for callers that cannot allocate device
+// memory.
+//
+// mhc_pre_bwd asks its caller for scratch (per-token records and the dphi
+// partials of each token block).  Some callers have no way to provide it: a
+// custom-op or plugin interface that hands the op its tensors but no
+// workspace, a runtime that plans all device memory ahead of time and forbids
+// allocation once it runs, or a latency-bound loop where cudaMalloc's implicit
+// device synchronisation is not acceptable.  This entry point takes its
+// scratch from a fixed-size array in the library's own device memory instead.
+//
+// The array is a file-scope __device__ variable, so every GPU that loads the
+// library holds it (MHC_PRE_BWD_NOALLOC_SCRATCH_BYTES) until the process
+// exits.  In host code its name is only a host-side stand-in, never a device
+// address: the device address is fetched with cudaGetSymbolAddress once per
+// device (with that device current) on the first call on that device, and
+// passed to the kernels.  All calls share the array and it keeps the last
+// call's contents; every kernel here writes each scratch element before it
+// reads it, so nothing needs clearing.  Calls that overlap on the GPU (for
+// example on two streams of one device) race on the array.
+#include <mutex>
+
+#include "../../include/mhc.h"
+#include "launch.h"
+
+namespace mhc {
+
+static __device__ __align__(256) unsigned char g_pre_bwd_scratch[MHC_PRE_BWD_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kLogits = 24;   // 2n + n^2 gate logits for n = 4
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mutex;
+void* g_scratch_ptr[kMaxDevices];
+
+// Device address of the scratch array on the current device (set up once per
+// device).  Returns nullptr if the device cannot be queried or the symbol
+// cannot be resolved.
+void* scratch_on_current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    if (g_scratch_ptr[dev] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_pre_bwd_scratch) != cudaSuccess) return nullptr;
+        g_scratch_ptr[dev] = ptr;
+    }
+    return g_scratch_ptr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace mhc
+
+extern "C" mhc_status mhc_pre_bwd_noalloc(mhc_dtype dt, const void* g_in, const float* dH_post,
+                                          const float* dH_res, const void* x, const float* phi,
+                                          const float* b, const float* alpha, const float* proj,
+                                          const float* inv_rms, int64_t T, int n, int64_t D,
+                                          int iters, void* dx, float* dphi, float* db,
+                                          float* dalpha, cudaStream_t stream) {
+    if (dt != MHC_F32 && dt != MHC_BF16) return MHC_ERR_INVALID_ARG;
+    if (T < 0 || D <= 0) return MHC_ERR_INVALID_ARG;
+    if (n != 4) return MHC_ERR_UNSUPPORTED;
+    if (D % (dt == MHC_BF16 ? 8 : 4) != 0) return MHC_ERR_UNSUPPORTED;
+    if (T > (int64_t(1) << 31) || D > (int64_t(1) << 24)) return MHC_ERR_UNSUPPORTED;
+    if (iters < 1) return MHC_ERR_INVALID_ARG;
+    if (iters > MHC_MAX_ITERS) return MHC_ERR_UNSUPPORTED;
+    if (T == 0) return MHC_OK;
+    const void* ptrs[] = {g_in, dH_post, dH_res, x, phi, b, alpha, proj, inv_rms, dx, dphi, db, dalpha};
+    for (const void* p : ptrs) {
+        if (p == nullptr) return MHC_ERR_INVALID_ARG;
+        if (!mhc::aligned16(p)) return MHC_ERR_MISALIGNED;
+    }
+    // Scratch plan: T per-token records, then as many dphi token blocks as
+    // both the usual plan and the fixed array allow (at least one).
+    const size_t rec_bytes = static_cast<size_t>(T) * mhc::REC * sizeof(float);
+    const size_t part_bytes = static_cast<size_t>(4 * D) * mhc::kLogits * sizeof(float);
+    const size_t cap = MHC_PRE_BWD_NOALLOC_SCRATCH_BYTES;
+    if (rec_bytes + part_bytes > cap) return MHC_ERR_UNSUPPORTED;   // too large for the array
+    int64_t nb = mhc::pre_bwd_plan(T, D).nb;
+    const int64_t fit = static_cast<int64_t>((cap - rec_bytes) / part_bytes);
+    if (nb > fit) nb = fit;
+    void* ws = mhc::scratch_on_current_device();
+    if (ws == nullptr) return MHC_ERR_CUDA;
+    const cudaError_t e = mhc::launch_pre_bwd_blocks(dt == MHC_BF16, g_in, dH_post, dH_res, x, phi, b,
+                                                     alpha, proj, inv_rms, T, D, iters, dx, dphi, db,
+                                                     dalpha, ws, nb, stream);
+    return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA;
+}

@@ -125,3 +125,20 @@ def test_binding_refuses_cpu_tensors():
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="no CPU path"):
         B.lib(str(tmp_path / "absent.so"))
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch(L):
+    # 16 MiB of scratch: T * 256 B of records plus one 4*D x 24 float partial
+    # must fit; the refusal comes before any CUDA call.
+    args = [A] * 9
+
+    def call(T, D):
+        return L.mhc_pre_bwd_noalloc(B.MHC_BF16, *args, T, 4, D, 20, A, A, A, A, None)
+
+    assert call(60000, 5120) == B.MHC_ERR_UNSUPPORTED
+    assert call(1 << 20, 64) == B.MHC_ERR_UNSUPPORTED
+    assert call(0, 5120) == B.MHC_OK
+    assert L.mhc_pre_bwd_noalloc(B.MHC_BF16, *args, 16, 4, 64, 0, A, A, A, A,
+                                 None) == B.MHC_ERR_INVALID_ARG
+    assert L.mhc_pre_bwd_noalloc(B.MHC_BF16, *args, 16, 4, 64, 20, MIS, A, A, A,
+                                 None) == B.MHC_ERR_MISALIGNED
