@@ -184,27 +184,36 @@ constexpr int MB_THREADS = 128;
 constexpr int MB_KS = 2 * MB_THREADS;   // K elements per CTA
 constexpr int MB_TCH = 32;              // tokens staged per chunk
 
+// Two consecutive activations of one token, kept in their storage form
+// (one 32-bit word for bf16, two floats for float32) until they are used.
 template <typename TA> struct Pair;
 template <> struct Pair<__nv_bfloat16> {
-    __device__ __forceinline__ static float2 load(const __nv_bfloat16* p) {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+    using Raw = uint32_t;
+    __device__ __forceinline__ static Raw load(const __nv_bfloat16* p) {
+        return *reinterpret_cast<const uint32_t*>(p);
+    }
+    __device__ __forceinline__ static float2 widen(Raw w) {
         return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
     }
     __device__ __forceinline__ static void store(__nv_bfloat16* p, float2 v) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
-        *reinterpret_cast<__nv_bfloat162*>(p) = h;
+        *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(v.x, v.y);
     }
 };
 template <> struct Pair<float> {
-    __device__ __forceinline__ static float2 load(const float* p) { return *reinterpret_cast<const float2*>(p); }
+    using Raw = float2;
+    __device__ __forceinline__ static Raw load(const float* p) { return *reinterpret_cast<const float2*>(p); }
+    __device__ __forceinline__ static float2 widen(Raw w) { return w; }
     __device__ __forceinline__ static void store(float* p, float2 v) { *reinterpret_cast<float2*>(p) = v; }
 };
+
+constexpr int MB_GROUP = 8;   // tokens whose loads are issued together
 
 template <typename TA>
 __global__ void __launch_bounds__(MB_THREADS)
 pre_bwd_main_kernel(const TA* __restrict__ g_in, const TA* __restrict__ x,
                     const float* __restrict__ phi, const float* __restrict__ rec, int64_t T,
                     int64_t D, int64_t tb, TA* __restrict__ dx, float* __restrict__ part) {
+    using P = Pair<TA>;
     __shared__ __align__(16) float rs[MB_TCH][32];   // u[24], H_pre[4], coef, pad
     const int64_t K = 4 * D;
     const int64_t k0 = static_cast<int64_t>(blockIdx.x) * MB_KS + 2 * threadIdx.x;
@@ -232,25 +241,44 @@ pre_bwd_main_kernel(const TA* __restrict__ g_in, const TA* __restrict__ x,
         }
         __syncthreads();
         if (!active) continue;
-        for (int tt = 0; tt < nt; ++tt) {
-            const int64_t t = c0 + tt;
-            const float2 xv = Pair<TA>::load(x + t * K + k0);
-            const float2 gv = Pair<TA>::load(g_in + t * D + d0);
-            const float2 dv = Pair<TA>::load(dx + t * K + k0);
-            const float* u = rs[tt];
-            const float hpre = u[REC_HPRE + si], coef = u[REC_COEF];
-            float s0 = 0.f, s1 = 0.f;
+        for (int tg = 0; tg < nt; tg += MB_GROUP) {
+            typename P::Raw xr[MB_GROUP], gr[MB_GROUP], dr[MB_GROUP];
 #pragma unroll
-            for (int g = 0; g < NG; ++g) {
-                s0 = fmaf(ph0[g], u[g], s0);
-                s1 = fmaf(ph1[g], u[g], s1);
-                acc0[g] = fmaf(xv.x, u[g], acc0[g]);
-                acc1[g] = fmaf(xv.y, u[g], acc1[g]);
+            for (int m = 0; m < MB_GROUP; ++m) {
+                if (tg + m < nt) {
+                    const int64_t t = c0 + tg + m;
+                    xr[m] = P::load(x + t * K + k0);
+                    gr[m] = P::load(g_in + t * D + d0);
+                    dr[m] = P::load(dx + t * K + k0);
+                }
             }
-            float2 o;
-            o.x = dv.x + fmaf(hpre, gv.x, fmaf(coef, xv.x, s0));
-            o.y = dv.y + fmaf(hpre, gv.y, fmaf(coef, xv.y, s1));
-            Pair<TA>::store(dx + t * K + k0, o);
+#pragma unroll
+            for (int m = 0; m < MB_GROUP; ++m) {
+                if (tg + m < nt) {
+                    const int64_t t = c0 + tg + m;
+                    const float2 xv = P::widen(xr[m]), gv = P::widen(gr[m]), dv = P::widen(dr[m]);
+                    const float4* u4 = reinterpret_cast<const float4*>(rs[tg + m]);
+                    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                    for (int v = 0; v < NG / 4; ++v) {
+                        const float4 u = u4[v];
+                        const float uu[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int g = 4 * v + e;
+                            s0 = fmaf(ph0[g], uu[e], s0);
+                            s1 = fmaf(ph1[g], uu[e], s1);
+                            acc0[g] = fmaf(xv.x, uu[e], acc0[g]);
+                            acc1[g] = fmaf(xv.y, uu[e], acc1[g]);
+                        }
+                    }
+                    const float hpre = rs[tg + m][REC_HPRE + si], coef = rs[tg + m][REC_COEF];
+                    float2 o;
+                    o.x = dv.x + fmaf(hpre, gv.x, fmaf(coef, xv.x, s0));
+                    o.y = dv.y + fmaf(hpre, gv.y, fmaf(coef, xv.y, s1));
+                    P::store(dx + t * K + k0, o);
+                }
+            }
         }
     }
     if (active) {
@@ -275,20 +303,26 @@ pre_bwd_reduce_phi_kernel(const float* __restrict__ part, int64_t nb, int64_t n4
     }
 }
 
-// 4b. db[g] = sum_t dlogits[t, g]; dalpha[c] = sum_t da[t, c].  One warp per
-//     output column, fixed summation order.
-__global__ void __launch_bounds__(1024)
+// 4b. db[g] = sum_t dlogits[t, g]; dalpha[c] = sum_t da[t, c].  One CTA per
+//     output column; each thread sums a strided subset of tokens, then a
+//     fixed-shape tree over the CTA (deterministic).
+__global__ void __launch_bounds__(256)
 pre_bwd_reduce_bias_kernel(const float* __restrict__ rec, int64_t T, float* __restrict__ db,
                            float* __restrict__ dalpha) {
-    const int lane = threadIdx.x & 31, col = threadIdx.x >> 5;
-    if (col >= NG + 3) return;
+    __shared__ float part_s[256 / 32];
+    const int col = blockIdx.x;
     const int off = col < NG ? REC_DL + col : REC_DA + (col - NG);
     float s = 0.f;
-    for (int64_t t = lane; t < T; t += 32) s += rec[t * REC + off];
+    for (int64_t t = threadIdx.x; t < T; t += 256) s += rec[t * REC + off];
     s = warp_sum(s);
-    if (lane == 0) {
-        if (col < NG) db[col] = s;
-        else dalpha[col - NG] = s;
+    if ((threadIdx.x & 31) == 0) part_s[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < 256 / 32; ++w) tot += part_s[w];
+        if (col < NG) db[col] = tot;
+        else dalpha[col - NG] = tot;
     }
 }
 
@@ -355,7 +389,7 @@ cudaError_t launch_pre_bwd(bool bf16, const void* g_in, const float* dH_post,
     const int64_t n4 = K * NG / 4;
     const dim3 gr(static_cast<unsigned>((n4 + 255) / 256 < 4096 ? (n4 + 255) / 256 : 4096));
     pre_bwd_reduce_phi_kernel<<<gr, 256, 0, s>>>(part, p.nb, n4, dphi);
-    pre_bwd_reduce_bias_kernel<<<1, 1024, 0, s>>>(rec, T, db, dalpha);
+    pre_bwd_reduce_bias_kernel<<<NG + 3, 256, 0, s>>>(rec, T, db, dalpha);
     return cudaGetLastError();
 }
 
@@ -393,7 +427,7 @@ cudaError_t launch_pre_bwd_blocks(bool bf16, const void* g_in, const float* dH_p
     const int64_t n4 = K * NG / 4;
     const dim3 gr(static_cast<unsigned>((n4 + 255) / 256 < 4096 ? (n4 + 255) / 256 : 4096));
     pre_bwd_reduce_phi_kernel<<<gr, 256, 0, s>>>(part, nb, n4, dphi);
-    pre_bwd_reduce_bias_kernel<<<1, 1024, 0, s>>>(rec, T, db, dalpha);
+    pre_bwd_reduce_bias_kernel<<<NG + 3, 256, 0, s>>>(rec, T, db, dalpha);
     return cudaGetLastError();
 }
 
