@@ -206,7 +206,44 @@ template <> struct Pair<float> {
     __device__ __forceinline__ static void store(float* p, float2 v) { *reinterpret_cast<float2*>(p) = v; }
 };
 
-constexpr int MB_GROUP = 8;   // tokens whose loads are issued together
+// cp.async of 4 or 8 bytes (zero fill when `valid` is false).
+template <int BYTES>
+__device__ __forceinline__ void cp_async_small(void* smem, const void* gmem, bool valid) {
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    const int n = valid ? BYTES : 0;
+    asm volatile("cp.async.ca.shared.global [%0], [%1], %2, %3;\n" ::"r"(s), "l"(gmem), "n"(BYTES), "r"(n)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_16(void* smem, const void* gmem, bool valid) {
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    const int n = valid ? 16 : 0;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_group() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+// Packed fused multiply-add on two float32 lanes (fma.rn.f32x2).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(r)
+        : "l"(*reinterpret_cast<unsigned long long*>(&a)), "l"(*reinterpret_cast<unsigned long long*>(&b)),
+          "l"(*reinterpret_cast<unsigned long long*>(&c)));
+    return *reinterpret_cast<float2*>(&r);
+}
+
+// Shared-memory pipeline of the main kernel: each stage holds MB_TS tokens'
+// records and, per thread, its two activations of x, g_in and dx.
+constexpr int MB_TS = 12;
+template <typename TA> struct MainCfg {
+    static constexpr int STAGES = sizeof(TA) == 2 ? 3 : 2;
+    static constexpr int RAW = 2 * static_cast<int>(sizeof(TA));          // bytes per thread per array
+    static constexpr int REC_BYTES = MB_TS * 32 * 4;
+    static constexpr int ARR_BYTES = MB_TS * MB_THREADS * RAW;
+    static constexpr int STAGE_BYTES = REC_BYTES + 3 * ARR_BYTES;
+    static constexpr int SMEM = STAGES * STAGE_BYTES;
+};
 
 template <typename TA>
 __global__ void __launch_bounds__(MB_THREADS)
@@ -214,77 +251,115 @@ pre_bwd_main_kernel(const TA* __restrict__ g_in, const TA* __restrict__ x,
                     const float* __restrict__ phi, const float* __restrict__ rec, int64_t T,
                     int64_t D, int64_t tb, TA* __restrict__ dx, float* __restrict__ part) {
     using P = Pair<TA>;
-    __shared__ __align__(16) float rs[MB_TCH][32];   // u[24], H_pre[4], coef, pad
+    using Raw = typename P::Raw;
+    using Cfg = MainCfg<TA>;
+    constexpr int S = Cfg::STAGES;
+    extern __shared__ __align__(16) unsigned char msm[];
+    const int tid = threadIdx.x;
     const int64_t K = 4 * D;
-    const int64_t k0 = static_cast<int64_t>(blockIdx.x) * MB_KS + 2 * threadIdx.x;
+    const int64_t k0 = static_cast<int64_t>(blockIdx.x) * MB_KS + 2 * tid;
     const bool active = k0 < K;
     const int si = active ? static_cast<int>(k0 / D) : 0;
     const int64_t d0 = active ? k0 - si * D : 0;
     const int64_t tbeg = static_cast<int64_t>(blockIdx.y) * tb;
     const int64_t tend = tbeg + tb < T ? tbeg + tb : T;
+    const int ntok = tend > tbeg ? static_cast<int>(tend - tbeg) : 0;
+    const int nst = (ntok + MB_TS - 1) / MB_TS;
 
-    float ph0[NG], ph1[NG], acc0[NG], acc1[NG];
+    auto st_rec = [&](int b) { return reinterpret_cast<float*>(msm + b * Cfg::STAGE_BYTES); };
+    auto st_arr = [&](int b, int a) {
+        return reinterpret_cast<Raw*>(msm + b * Cfg::STAGE_BYTES + Cfg::REC_BYTES + a * Cfg::ARR_BYTES);
+    };
+    auto issue = [&](int st) {
+        const int b = st % S;
+        const int64_t c0 = tbeg + static_cast<int64_t>(st) * MB_TS;
+        float* r = st_rec(b);
+        for (int q = tid; q < MB_TS * 8; q += MB_THREADS) {
+            const int tt = q >> 3, v = q & 7;
+            const bool ok = c0 + tt < tend;
+            cp_async_16(r + tt * 32 + v * 4, ok ? rec + (c0 + tt) * REC + v * 4 : rec, ok);
+        }
+        Raw* xa = st_arr(b, 0);
+        Raw* ga = st_arr(b, 1);
+        Raw* da = st_arr(b, 2);
+#pragma unroll 4
+        for (int tt = 0; tt < MB_TS; ++tt) {
+            const int64_t t = c0 + tt;
+            const bool ok = active && t < tend;
+            cp_async_small<sizeof(Raw)>(xa + tt * MB_THREADS + tid, ok ? x + t * K + k0 : x, ok);
+            cp_async_small<sizeof(Raw)>(ga + tt * MB_THREADS + tid, ok ? g_in + t * D + d0 : g_in, ok);
+            cp_async_small<sizeof(Raw)>(da + tt * MB_THREADS + tid, ok ? dx + t * K + k0 : dx, ok);
+        }
+    };
+
+    // phi rows k0, k0+1 and the dphi accumulators, paired per logit g
+    float2 ph[NG], acc[NG];
 #pragma unroll
     for (int g = 0; g < NG; ++g) {
-        ph0[g] = active ? phi[k0 * NG + g] : 0.f;
-        ph1[g] = active ? phi[(k0 + 1) * NG + g] : 0.f;
-        acc0[g] = acc1[g] = 0.f;
+        ph[g] = active ? make_float2(phi[k0 * NG + g], phi[(k0 + 1) * NG + g]) : make_float2(0.f, 0.f);
+        acc[g] = make_float2(0.f, 0.f);
     }
-    for (int64_t c0 = tbeg; c0 < tend; c0 += MB_TCH) {
-        const int nt = static_cast<int>(tend - c0 < MB_TCH ? tend - c0 : MB_TCH);
-        __syncthreads();
-        for (int q = threadIdx.x; q < MB_TCH * 8; q += MB_THREADS) {
-            const int tt = q >> 3, v = q & 7;
-            float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (tt < nt) val = reinterpret_cast<const float4*>(rec + (c0 + tt) * REC)[v];
-            reinterpret_cast<float4*>(&rs[tt][0])[v] = val;
-        }
-        __syncthreads();
-        if (!active) continue;
-        for (int tg = 0; tg < nt; tg += MB_GROUP) {
-            typename P::Raw xr[MB_GROUP], gr[MB_GROUP], dr[MB_GROUP];
 #pragma unroll
-            for (int m = 0; m < MB_GROUP; ++m) {
-                if (tg + m < nt) {
-                    const int64_t t = c0 + tg + m;
-                    xr[m] = P::load(x + t * K + k0);
-                    gr[m] = P::load(g_in + t * D + d0);
-                    dr[m] = P::load(dx + t * K + k0);
-                }
-            }
+    for (int st = 0; st < S - 1; ++st) {
+        if (st < nst) issue(st);
+        cp_async_commit_group();
+    }
+    for (int st = 0; st < nst; ++st) {
+        cp_async_wait_group<S - 2>();
+        __syncthreads();   // stage st landed for every thread; stage st-1 is free
+        if (st + S - 1 < nst) issue(st + S - 1);
+        cp_async_commit_group();
+        const int b = st % S;
+        const float* r = st_rec(b);
+        const Raw* xa = st_arr(b, 0);
+        const Raw* ga = st_arr(b, 1);
+        const Raw* da = st_arr(b, 2);
+        const int64_t c0 = tbeg + static_cast<int64_t>(st) * MB_TS;
+        const int nt = static_cast<int>(tend - c0 < MB_TS ? tend - c0 : MB_TS);
+        if (active) {
+            for (int tt = 0; tt < nt; ++tt) {
+                const float2 xv = P::widen(xa[tt * MB_THREADS + tid]);
+                const float2 gv = P::widen(ga[tt * MB_THREADS + tid]);
+                const float2 dv = P::widen(da[tt * MB_THREADS + tid]);
+                const float4* u4 = reinterpret_cast<const float4*>(r + tt * 32);
+                float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);   // (phi u) for k0, k0+1
 #pragma unroll
-            for (int m = 0; m < MB_GROUP; ++m) {
-                if (tg + m < nt) {
-                    const int64_t t = c0 + tg + m;
-                    const float2 xv = P::widen(xr[m]), gv = P::widen(gr[m]), dv = P::widen(dr[m]);
-                    const float4* u4 = reinterpret_cast<const float4*>(rs[tg + m]);
-                    float s0 = 0.f, s1 = 0.f;
+                for (int v = 0; v < NG / 4; ++v) {
+                    const float4 u = u4[v];
+                    const float uu[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                    for (int v = 0; v < NG / 4; ++v) {
-                        const float4 u = u4[v];
-                        const float uu[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int g = 4 * v + e;
-                            s0 = fmaf(ph0[g], uu[e], s0);
-                            s1 = fmaf(ph1[g], uu[e], s1);
-                            acc0[g] = fmaf(xv.x, uu[e], acc0[g]);
-                            acc1[g] = fmaf(xv.y, uu[e], acc1[g]);
-                        }
+                    for (int e = 0; e < 4; ++e) {
+                        const int g = 4 * v + e;
+                        const float2 u2 = make_float2(uu[e], uu[e]);
+                        if (e & 1) sb = ffma2(ph[g], u2, sb);
+                        else sa = ffma2(ph[g], u2, sa);
+                        acc[g] = ffma2(xv, u2, acc[g]);
                     }
-                    const float hpre = rs[tg + m][REC_HPRE + si], coef = rs[tg + m][REC_COEF];
-                    float2 o;
-                    o.x = dv.x + fmaf(hpre, gv.x, fmaf(coef, xv.x, s0));
-                    o.y = dv.y + fmaf(hpre, gv.y, fmaf(coef, xv.y, s1));
-                    P::store(dx + t * K + k0, o);
                 }
+                const float s0 = sa.x + sb.x, s1 = sa.y + sb.y;
+                const float hpre = r[tt * 32 + REC_HPRE + si], coef = r[tt * 32 + REC_COEF];
+                float2 o;
+                o.x = dv.x + fmaf(hpre, gv.x, fmaf(coef, xv.x, s0));
+                o.y = dv.y + fmaf(hpre, gv.y, fmaf(coef, xv.y, s1));
+                P::store(dx + (c0 + tt) * K + k0, o);
             }
         }
     }
+    cp_async_wait_group<0>();
     if (active) {
         float* p = part + (static_cast<int64_t>(blockIdx.y) * K + k0) * NG;
 #pragma unroll
-        for (int g = 0; g < NG; ++g) { p[g] = acc0[g]; p[NG + g] = acc1[g]; }
+        for (int g = 0; g < NG; ++g) { p[g] = acc[g].x; p[NG + g] = acc[g].y; }
+    }
+}
+
+template <typename TA>
+void set_main_smem_once() {
+    static bool done = false;   // the attribute is per function and context-wide
+    if (!done) {
+        cudaFuncSetAttribute(pre_bwd_main_kernel<TA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             MainCfg<TA>::SMEM);
+        done = true;
     }
 }
 
@@ -375,14 +450,21 @@ cudaError_t launch_pre_bwd(bool bf16, const void* g_in, const float* dH_post,
         pre_bwd_dots_kernel<__nv_bfloat16><<<gw, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(g_in),
                                                               static_cast<const __nv_bfloat16*>(x), T, D, rec);
         pre_bwd_token_kernel<<<gt, 128, 0, s>>>(dH_post, dH_res, b, alpha, proj, inv_rms, T, K, iters, rec);
-        pre_bwd_main_kernel<__nv_bfloat16><<<gm, MB_THREADS, 0, s>>>(
-            static_cast<const __nv_bfloat16*>(g_in), static_cast<const __nv_bfloat16*>(x), phi, rec, T, D,
-            p.tb, static_cast<__nv_bfloat16*>(dx), part);
+        if (pre_bwd_tc_supports(T, D)) {
+            const cudaError_t e = launch_pre_bwd_tc_main(g_in, x, phi, rec, T, D, p.nb, dx, part, s);
+            if (e != cudaSuccess) return e;
+        } else {
+            set_main_smem_once<__nv_bfloat16>();
+            pre_bwd_main_kernel<__nv_bfloat16><<<gm, MB_THREADS, MainCfg<__nv_bfloat16>::SMEM, s>>>(
+                static_cast<const __nv_bfloat16*>(g_in), static_cast<const __nv_bfloat16*>(x), phi, rec, T, D,
+                p.tb, static_cast<__nv_bfloat16*>(dx), part);
+        }
     } else {
         pre_bwd_dots_kernel<float><<<gw, 256, 0, s>>>(static_cast<const float*>(g_in),
                                                       static_cast<const float*>(x), T, D, rec);
         pre_bwd_token_kernel<<<gt, 128, 0, s>>>(dH_post, dH_res, b, alpha, proj, inv_rms, T, K, iters, rec);
-        pre_bwd_main_kernel<float><<<gm, MB_THREADS, 0, s>>>(static_cast<const float*>(g_in),
+        set_main_smem_once<float>();
+        pre_bwd_main_kernel<float><<<gm, MB_THREADS, MainCfg<float>::SMEM, s>>>(static_cast<const float*>(g_in),
                                                              static_cast<const float*>(x), phi, rec, T, D,
                                                              p.tb, static_cast<float*>(dx), part);
     }
@@ -413,14 +495,21 @@ cudaError_t launch_pre_bwd_blocks(bool bf16, const void* g_in, const float* dH_p
         pre_bwd_dots_kernel<__nv_bfloat16><<<gw, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(g_in),
                                                               static_cast<const __nv_bfloat16*>(x), T, D, rec);
         pre_bwd_token_kernel<<<gt, 128, 0, s>>>(dH_post, dH_res, b, alpha, proj, inv_rms, T, K, iters, rec);
-        pre_bwd_main_kernel<__nv_bfloat16><<<gm, MB_THREADS, 0, s>>>(
-            static_cast<const __nv_bfloat16*>(g_in), static_cast<const __nv_bfloat16*>(x), phi, rec, T, D,
-            tb, static_cast<__nv_bfloat16*>(dx), part);
+        if (pre_bwd_tc_supports(T, D)) {
+            const cudaError_t e = launch_pre_bwd_tc_main(g_in, x, phi, rec, T, D, nb, dx, part, s);
+            if (e != cudaSuccess) return e;
+        } else {
+            set_main_smem_once<__nv_bfloat16>();
+            pre_bwd_main_kernel<__nv_bfloat16><<<gm, MB_THREADS, MainCfg<__nv_bfloat16>::SMEM, s>>>(
+                static_cast<const __nv_bfloat16*>(g_in), static_cast<const __nv_bfloat16*>(x), phi, rec, T, D,
+                tb, static_cast<__nv_bfloat16*>(dx), part);
+        }
     } else {
         pre_bwd_dots_kernel<float><<<gw, 256, 0, s>>>(static_cast<const float*>(g_in),
                                                       static_cast<const float*>(x), T, D, rec);
         pre_bwd_token_kernel<<<gt, 128, 0, s>>>(dH_post, dH_res, b, alpha, proj, inv_rms, T, K, iters, rec);
-        pre_bwd_main_kernel<float><<<gm, MB_THREADS, 0, s>>>(static_cast<const float*>(g_in),
+        set_main_smem_once<float>();
+        pre_bwd_main_kernel<float><<<gm, MB_THREADS, MainCfg<float>::SMEM, s>>>(static_cast<const float*>(g_in),
                                                              static_cast<const float*>(x), phi, rec, T, D,
                                                              tb, static_cast<float*>(dx), part);
     }

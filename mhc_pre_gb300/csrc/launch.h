@@ -56,4 +56,10 @@ cudaError_t launch_pre_bwd_blocks(bool bf16, const void* g_in, const float* dH_p
                                   float* dphi, float* db, float* dalpha, void* ws, int64_t nb,
                                   cudaStream_t s);
 
+// Tensor-core main step of the pre backward (bf16; pre_bwd_tc.cu).
+bool pre_bwd_tc_supports(int64_t T, int64_t D);
+cudaError_t launch_pre_bwd_tc_main(const void* g_in, const void* x, const float* phi, const float* rec,
+                                   int64_t T, int64_t D, int64_t nb, void* dx, float* part,
+                                   cudaStream_t s);
+
 }  // namespace mhc

@@ -42,13 +42,20 @@ namespace mhc {
 // mhc_get_last_device_error().
 __device__ unsigned g_device_error;
 
+cudaError_t read_and_clear_bwd_tc_error(unsigned* word);   // pre_bwd_tc.cu
+
 cudaError_t read_and_clear_device_error(unsigned* word, cudaStream_t s) {
     cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return e;
     e = cudaMemcpyFromSymbol(word, g_device_error, sizeof(unsigned));
     if (e != cudaSuccess) return e;
     const unsigned zero = 0;
-    return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(unsigned));
+    e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    unsigned other = 0;
+    e = read_and_clear_bwd_tc_error(&other);
+    *word |= other;
+    return e;
 }
 
 namespace tc {
@@ -572,6 +579,8 @@ cudaError_t launch(const CUtensorMap& tm, const Params& prm, int nclusters, size
 }
 
 }  // namespace tc
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() { return tc::encode_fn(); }
 
 bool pre_tc_supports(int64_t T, int64_t D) {
     if (T < tc::TILE_M || D > (int64_t(1) << 20)) return false;
