@@ -329,17 +329,36 @@ def launches(w):
     return sum(B.kernel_launches(op, w.dtype, w.T, w.n, w.D) for op in STEP_OPS)
 
 
+def kernel_sources_sha256():
+    import glob
+    import hashlib
+    csrc = os.path.join(ROOT, "mhc_pre_gb300", "csrc")
+    files = sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))
+                   + glob.glob(os.path.join(csrc, "*.h")))
+    h = hashlib.sha256()
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def ncu_traffic(op, w):
-    """DRAM bytes per launch of ``op`` from the committed ncu summary, scaled
-    to this workload's token count; None when no current capture exists."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    """DRAM bytes per launch of ``op`` from the committed ncu summary (per
+    token, scaled to this workload); None when the summary was taken on
+    other kernel sources or another width."""
+    import re
+    path = os.path.join(ROOT, "profiles", "step_T32768_D5120_launches_dram.md")
     try:
         with open(path) as f:
-            d = json.load(f)
-        rec = d[op]
-        return rec["bytes_per_token"] * w.T + rec.get("bytes_per_launch_fixed", 0)
-    except (OSError, KeyError, ValueError):
+            text = f.read()
+    except OSError:
         return None
+    m = re.search(r"sources_sha256: ([0-9a-f]{64})", text)
+    if m is None or m.group(1) != kernel_sources_sha256() or w.D != 5120 or w.n != 4:
+        return None
+    m = re.search(r"traffic_per_token %s (\d+)" % re.escape(op), text)
+    return int(m.group(1)) * w.T if m else None
 
 
 def run_e2e(args, w, inp, step, stream, dev, world):
