@@ -205,6 +205,7 @@ def main():
     from mhc_pre_gb300 import binding as B
     from mhc_pre_gb300 import build as mbuild
     from mhc_pre_gb300 import workloads as W
+    from mhc_pre_gb300.dp import allreduce_param_grads
 
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
@@ -234,8 +235,7 @@ def main():
                            inp["alpha"], f.proj, f.inv_rms, pb.dx, w.iters, workspace=ws)
         if e: e[4].record(stream)
         if world > 1:
-            flat = torch.cat([qb.dphi.view(-1), qb.db, qb.dalpha])
-            dist.all_reduce(flat)
+            allreduce_param_grads(qb.dphi, qb.db, qb.dalpha)
         return qb
 
     for _ in range(args.warmup):

@@ -151,6 +151,12 @@ size_t mhc_pre_bwd_workspace_bytes(mhc_dtype dt, int64_t T, int n, int64_t D);
  *   dalpha  [3]        float   written
  *   workspace, ws_bytes        device scratch of at least
  *                              mhc_pre_bwd_workspace_bytes() bytes
+ *
+ * Data parallelism: dphi, db and dalpha are sums over this call's tokens, so
+ * ranks that each hold a slice of the batch add them (one all-reduce) to get
+ * the full-batch gradient; every other output is per token.  For T = 0
+ * nothing is written, not even dphi, db and dalpha: a caller that takes part
+ * in such a sum with no tokens sets them to zero itself.
  */
 mhc_status mhc_pre_bwd(mhc_dtype dt, const void* g_in, const float* dH_post,
                        const float* dH_res, const void* x, const float* phi,

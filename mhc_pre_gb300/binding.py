@@ -196,6 +196,9 @@ def mhc_pre_bwd(g_in, dH_post, dH_res, x, phi, b, alpha, proj, inv_rms, dx,
                            _ptr(workspace), workspace.numel() * workspace.element_size(),
                            _stream(x.device))
     _check(st, "mhc_pre_bwd")
+    if T == 0:  # the library writes nothing for an empty batch; its gradient is zero
+        for t in (dphi, db, dalpha):
+            t.zero_()
     return PreBwdOut(dx, dphi, db, dalpha)
 
 
@@ -219,6 +222,9 @@ def mhc_pre_bwd_noalloc(g_in, dH_post, dH_res, x, phi, b, alpha, proj, inv_rms,
         _ptr(_f32(proj, "proj")), _ptr(_f32(inv_rms, "inv_rms")), T, n, D, iters, _ptr(dx),
         _ptr(dphi), _ptr(db), _ptr(dalpha), _stream(x.device))
     _check(st, "mhc_pre_bwd_noalloc")
+    if T == 0:
+        for t in (dphi, db, dalpha):
+            t.zero_()
     return PreBwdOut(dx, dphi, db, dalpha)
 
 

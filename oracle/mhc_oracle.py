@@ -58,8 +58,8 @@ def rmsnorm_flat(x, eps: float):
     inv_rms = 1 / sqrt(mean(x^2) + eps).
     """
     x = _f64(x)
-    T = x.shape[0]
-    flat = x.reshape(T, -1)
+    T, n, D = x.shape
+    flat = x.reshape(T, n * D)
     ms = np.mean(flat * flat, axis=1)
     inv_rms = 1.0 / np.sqrt(ms + eps)
     return x * inv_rms[:, None, None], inv_rms
@@ -71,8 +71,8 @@ def project(x_bar, phi):
     x_bar: [T, n, D]; phi: [n*D, G] (row k = i*D + d).  Returns [T, G].
     """
     x_bar = _f64(x_bar)
-    T = x_bar.shape[0]
-    return x_bar.reshape(T, -1) @ _f64(phi)
+    T, n, D = x_bar.shape
+    return x_bar.reshape(T, n * D) @ _f64(phi)
 
 
 def logits_from_proj(proj, alpha, b, n: int):

@@ -101,6 +101,15 @@ def test_empty_batch_is_a_noop():
     assert f.x_in.shape == (0, 64)
     xn = B.mhc_post(x, torch.empty((0, 64), dtype=torch.bfloat16, device=dev), f.H_post, f.H_res)
     assert xn.shape == (0, 4, 64)
+    # an empty batch contributes zero parameter gradient (a data-parallel rank
+    # with no tokens still takes part in the sum)
+    e = torch.empty((0, 4), device=dev)
+    qb = B.mhc_pre_bwd(torch.empty((0, 64), dtype=torch.bfloat16, device=dev), e,
+                       torch.empty((0, 4, 4), device=dev), x, phi, torch.zeros(24, device=dev),
+                       torch.zeros(3, device=dev), torch.empty((0, 24), device=dev),
+                       torch.empty((0,), device=dev), torch.empty_like(x))
+    for t in (qb.dphi, qb.db, qb.dalpha):
+        assert torch.count_nonzero(t).item() == 0
 
 
 def test_invariants_hold_on_gpu_output():
