@@ -43,6 +43,8 @@ def parse_args():
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--workload", type=int, default=5)
     p.add_argument("--iters", type=int, default=20)
+    p.add_argument("--tokens", type=int, default=None,
+                   help="override the workload's T (smaller cases for profiling)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     return p.parse_args()
@@ -215,6 +217,8 @@ def main():
     mbuild.build()
 
     w = W.WORKLOADS[args.workload].with_(iters=args.iters, backward=True)
+    if args.tokens is not None:
+        w = w.with_(T=args.tokens)
     inp = W.make_inputs(w, device=dev, seed=1000 + w.wid + 7919 * rank)
     ws = torch.empty((max(B.pre_bwd_workspace_bytes(torch.bfloat16, w.T, w.n, w.D), 16),),
                      dtype=torch.uint8, device=dev)
@@ -288,7 +292,7 @@ def main():
 
     # ---- float64 oracle on the host cores (rank 0, N = 1) --------------------
     cpu = None
-    if rank == 0 and world == 1:
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
         rate, done, el = oracle_rate(w, args.cpu_seconds)
         cpu = {"value": rate, "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
                "kind": "oracle",

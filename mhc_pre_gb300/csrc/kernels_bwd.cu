@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(128)
 pre_bwd_token_kernel(const float* __restrict__ dH_post, const float* __restrict__ dH_res,
                      const float* __restrict__ b, const float* __restrict__ alpha,
                      const float* __restrict__ proj, const float* __restrict__ inv_rms, int64_t T,
-                     int64_t K, int iters, float* __restrict__ rec) {
+                     int64_t K, int iters, int have_dhpre, float* __restrict__ rec) {
     const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (t >= T) return;
     float* r = rec + t * REC;
@@ -138,17 +138,21 @@ pre_bwd_token_kernel(const float* __restrict__ dH_post, const float* __restrict_
     }
     float lg[NG];
     make_logits(pj, alpha, b, lg);
-    const float4 dhp4 = reinterpret_cast<const float4*>(r + REC_DHPRE)[0];
+    // without dH_pre (the one-pass kernel computes it later) the pre gates'
+    // terms are left at zero here and completed there
+    const float4 dhp4 = have_dhpre ? reinterpret_cast<const float4*>(r + REC_DHPRE)[0]
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
     const float4 dhq4 = reinterpret_cast<const float4*>(dH_post)[t];
     const float dhp[4] = {dhp4.x, dhp4.y, dhp4.z, dhp4.w};
     const float dhq[4] = {dhq4.x, dhq4.y, dhq4.z, dhq4.w};
-    float dl[NG], hpre[4];
+    float dl[NG], hpre[4], dsig[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const float sp = sigmoid_f(lg[i]);
         const float sq = sigmoid_f(lg[NS + i]);
         hpre[i] = sp;
-        dl[i] = dhp[i] * sp * (1.0f - sp);
+        dsig[i] = sp * (1.0f - sp);
+        dl[i] = dhp[i] * dsig[i];
         dl[NS + i] = dhq[i] * 2.0f * sq * (1.0f - sq);
     }
     float dhr[16];
@@ -174,6 +178,8 @@ pre_bwd_token_kernel(const float* __restrict__ dH_post, const float* __restrict_
 #pragma unroll
     for (int i = 0; i < 4; ++i) r[REC_HPRE + i] = hpre[i];
     r[REC_COEF] = -s * s * vp / static_cast<float>(K);
+    r[REC_S] = s;
+    reinterpret_cast<float4*>(r + REC_DSIG)[0] = make_float4(dsig[0], dsig[1], dsig[2], dsig[3]);
 #pragma unroll
     for (int c = 0; c < 3; ++c) r[REC_DA + c] = da[c];
 }
@@ -434,50 +440,9 @@ cudaError_t launch_post_bwd(bool bf16, const void* g, const void* x, const void*
     return cudaGetLastError();
 }
 
-cudaError_t launch_pre_bwd(bool bf16, const void* g_in, const float* dH_post,
-                           const float* dH_res, const void* x, const float* phi, const float* b,
-                           const float* alpha, const float* proj, const float* inv_rms, int64_t T,
-                           int64_t D, int iters, void* dx, float* dphi, float* db, float* dalpha,
-                           void* ws, cudaStream_t s) {
-    const PreBwdPlan p = pre_bwd_plan(T, D);
-    const int64_t K = 4 * D;
-    float* rec = static_cast<float*>(ws);
-    float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + p.rec_bytes);
-    const dim3 gw(static_cast<unsigned>((T * 32 + 255) / 256));
-    const dim3 gt(static_cast<unsigned>((T + 127) / 128));
-    const dim3 gm(static_cast<unsigned>((K + MB_KS - 1) / MB_KS), static_cast<unsigned>(p.nb));
-    if (bf16) {
-        pre_bwd_dots_kernel<__nv_bfloat16><<<gw, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(g_in),
-                                                              static_cast<const __nv_bfloat16*>(x), T, D, rec);
-        pre_bwd_token_kernel<<<gt, 128, 0, s>>>(dH_post, dH_res, b, alpha, proj, inv_rms, T, K, iters, rec);
-        if (pre_bwd_tc_supports(T, D)) {
-            const cudaError_t e = launch_pre_bwd_tc_main(g_in, x, phi, rec, T, D, p.nb, dx, part, s);
-            if (e != cudaSuccess) return e;
-        } else {
-            set_main_smem_once<__nv_bfloat16>();
-            pre_bwd_main_kernel<__nv_bfloat16><<<gm, MB_THREADS, MainCfg<__nv_bfloat16>::SMEM, s>>>(
-                static_cast<const __nv_bfloat16*>(g_in), static_cast<const __nv_bfloat16*>(x), phi, rec, T, D,
-                p.tb, static_cast<__nv_bfloat16*>(dx), part);
-        }
-    } else {
-        pre_bwd_dots_kernel<float><<<gw, 256, 0, s>>>(static_cast<const float*>(g_in),
-                                                      static_cast<const float*>(x), T, D, rec);
-        pre_bwd_token_kernel<<<gt, 128, 0, s>>>(dH_post, dH_res, b, alpha, proj, inv_rms, T, K, iters, rec);
-        set_main_smem_once<float>();
-        pre_bwd_main_kernel<float><<<gm, MB_THREADS, MainCfg<float>::SMEM, s>>>(static_cast<const float*>(g_in),
-                                                             static_cast<const float*>(x), phi, rec, T, D,
-                                                             p.tb, static_cast<float*>(dx), part);
-    }
-    const int64_t n4 = K * NG / 4;
-    const dim3 gr(static_cast<unsigned>((n4 + 255) / 256 < 4096 ? (n4 + 255) / 256 : 4096));
-    pre_bwd_reduce_phi_kernel<<<gr, 256, 0, s>>>(part, p.nb, n4, dphi);
-    pre_bwd_reduce_bias_kernel<<<NG + 3, 256, 0, s>>>(rec, T, db, dalpha);
-    return cudaGetLastError();
-}
-
-// The same launch sequence with the number of dphi token blocks chosen by
-// the caller (scratch = T * REC floats of records, then nb * K * NG floats of
-// partials); used by the entry point whose scratch has a fixed size.
+// The pre backward with room for at most nb dphi partials (scratch = T * REC
+// floats of records, then nb * K * NG floats of partials): launch_pre_bwd
+// passes the plan's nb, the entry point with a fixed scratch array its own.
 cudaError_t launch_pre_bwd_blocks(bool bf16, const void* g_in, const float* dH_post,
                                   const float* dH_res, const void* x, const float* phi,
                                   const float* b, const float* alpha, const float* proj,
@@ -491,10 +456,18 @@ cudaError_t launch_pre_bwd_blocks(bool bf16, const void* g_in, const float* dH_p
     const dim3 gw(static_cast<unsigned>((T * 32 + 255) / 256));
     const dim3 gt(static_cast<unsigned>((T + 127) / 128));
     const dim3 gm(static_cast<unsigned>((K + MB_KS - 1) / MB_KS), static_cast<unsigned>(nb));
-    if (bf16) {
+    int64_t nparts = nb;
+    if (bf16 && pre_bwd_fused_supports(T, D)) {
+        // one pass: per-token gate backward first (it does not need dH_pre),
+        // then the cluster kernel finds dH_pre and does the rest
+        pre_bwd_token_kernel<<<gt, 128, 0, s>>>(dH_post, dH_res, b, alpha, proj, inv_rms, T, K, iters, 0, rec);
+        const cudaError_t e = launch_pre_bwd_fused_main(g_in, x, phi, proj, alpha, rec, T, D, nb, dx, part,
+                                                        &nparts, s);
+        if (e != cudaSuccess) return e;
+    } else if (bf16) {
         pre_bwd_dots_kernel<__nv_bfloat16><<<gw, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(g_in),
                                                               static_cast<const __nv_bfloat16*>(x), T, D, rec);
-        pre_bwd_token_kernel<<<gt, 128, 0, s>>>(dH_post, dH_res, b, alpha, proj, inv_rms, T, K, iters, rec);
+        pre_bwd_token_kernel<<<gt, 128, 0, s>>>(dH_post, dH_res, b, alpha, proj, inv_rms, T, K, iters, 1, rec);
         if (pre_bwd_tc_supports(T, D)) {
             const cudaError_t e = launch_pre_bwd_tc_main(g_in, x, phi, rec, T, D, nb, dx, part, s);
             if (e != cudaSuccess) return e;
@@ -507,7 +480,7 @@ cudaError_t launch_pre_bwd_blocks(bool bf16, const void* g_in, const float* dH_p
     } else {
         pre_bwd_dots_kernel<float><<<gw, 256, 0, s>>>(static_cast<const float*>(g_in),
                                                       static_cast<const float*>(x), T, D, rec);
-        pre_bwd_token_kernel<<<gt, 128, 0, s>>>(dH_post, dH_res, b, alpha, proj, inv_rms, T, K, iters, rec);
+        pre_bwd_token_kernel<<<gt, 128, 0, s>>>(dH_post, dH_res, b, alpha, proj, inv_rms, T, K, iters, 1, rec);
         set_main_smem_once<float>();
         pre_bwd_main_kernel<float><<<gm, MB_THREADS, MainCfg<float>::SMEM, s>>>(static_cast<const float*>(g_in),
                                                              static_cast<const float*>(x), phi, rec, T, D,
@@ -515,9 +488,18 @@ cudaError_t launch_pre_bwd_blocks(bool bf16, const void* g_in, const float* dH_p
     }
     const int64_t n4 = K * NG / 4;
     const dim3 gr(static_cast<unsigned>((n4 + 255) / 256 < 4096 ? (n4 + 255) / 256 : 4096));
-    pre_bwd_reduce_phi_kernel<<<gr, 256, 0, s>>>(part, nb, n4, dphi);
+    pre_bwd_reduce_phi_kernel<<<gr, 256, 0, s>>>(part, nparts, n4, dphi);
     pre_bwd_reduce_bias_kernel<<<NG + 3, 256, 0, s>>>(rec, T, db, dalpha);
     return cudaGetLastError();
+}
+
+cudaError_t launch_pre_bwd(bool bf16, const void* g_in, const float* dH_post,
+                           const float* dH_res, const void* x, const float* phi, const float* b,
+                           const float* alpha, const float* proj, const float* inv_rms, int64_t T,
+                           int64_t D, int iters, void* dx, float* dphi, float* db, float* dalpha,
+                           void* ws, cudaStream_t s) {
+    return launch_pre_bwd_blocks(bf16, g_in, dH_post, dH_res, x, phi, b, alpha, proj, inv_rms, T, D, iters,
+                                 dx, dphi, db, dalpha, ws, pre_bwd_plan(T, D).nb, s);
 }
 
 }  // namespace mhc

@@ -15,7 +15,9 @@ constexpr int REC_HPRE = 24;    // [24, 28) H_pre
 constexpr int REC_COEF = 28;    // 28       coefficient of x in the RMSNorm backward
 constexpr int REC_DL = 32;      // [32, 56) dlogits
 constexpr int REC_DA = 56;      // [56, 59) per-token dalpha terms
-constexpr int REC_DHPRE = 60;   // [60, 64) dH_pre
+constexpr int REC_DHPRE = 60;   // [60, 64) dH_pre (input of the per-token kernel), then
+constexpr int REC_DSIG = 60;    //          s_i (1 - s_i) of the pre gates (its output)
+constexpr int REC_S = 29;       // 29       inv_rms
 
 // Sizes of the pre backward's dphi partial reduction.
 struct PreBwdPlan {
@@ -55,6 +57,16 @@ cudaError_t launch_pre_bwd_blocks(bool bf16, const void* g_in, const float* dH_p
                                   const float* inv_rms, int64_t T, int64_t D, int iters, void* dx,
                                   float* dphi, float* db, float* dalpha, void* ws, int64_t nb,
                                   cudaStream_t s);
+
+// One-pass cluster kernel of the pre backward (bf16; pre_bwd_fused.cu): the
+// dH_pre dots, the rest of u and the RMSNorm coefficient, dx and the dphi
+// partials (one per cluster, at most `max_parts`).  It expects records from
+// the per-token kernel run without dH_pre and writes their pre-gate parts.
+bool pre_bwd_fused_supports(int64_t T, int64_t D);
+cudaError_t launch_pre_bwd_fused_main(const void* g_in, const void* x, const float* phi,
+                                      const float* proj, const float* alpha, float* rec,
+                                      int64_t T, int64_t D, int64_t max_parts, void* dx,
+                                      float* part, int64_t* nparts, cudaStream_t s);
 
 // Tensor-core main step of the pre backward (bf16; pre_bwd_tc.cu).
 bool pre_bwd_tc_supports(int64_t T, int64_t D);

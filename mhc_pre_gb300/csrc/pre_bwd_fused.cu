@@ -1,0 +1,798 @@
+// pre_bwd_fused.cu -- one-pass tensor-core pre backward of the mHC layer
+// (bf16, n = 4) on thread-block clusters.
+//
+// What it computes, per token t (the layer of section 5.3 of the "openPangu
+// 2.0 -- architecture, training and Ascend systems" notes, differentiated;
+// the gates are recomputed from the saved projection as in the recompute
+// paragraph of the Ascend mHC Triton operator article):
+//   dH_pre[i] = <g_in, x[i]>,   dl_pre[i] = dH_pre[i] s_i (1 - s_i)
+//   u_pre[i]  = inv_rms alpha_pre dl_pre[i]
+//   coef      = coef_rest - inv_rms (u_pre . proj_pre) / K
+//   dx[t, k] += H_pre[i(k)] g_in[t, d(k)] + (phi u_t)[k] + coef x[t, k]
+//   dphi_part[k, g] = sum_t x[t, k] u[t, g]
+// The other 20 entries of u, coef_rest (the post and residual gates'
+// share of the RMSNorm coefficient) and the Sinkhorn backward come from the
+// per-token kernel that runs first: none of them depends on dH_pre.
+//
+// Design (GB300, one CTA per SM, persistent):
+//   * A cluster of C CTAs owns a tile of 64 tokens at a time; CTA r owns the
+//     columns d in [r*Dc, (r+1)*Dc) of every stream (Dc = 64 * nck).
+//   * First pass: TMA brings the tile's x (one 32 KB box: 4 streams x 64
+//     tokens x 64 columns) and g_in (8 KB) per 64-column chunk; four warps
+//     sum g_in * x[i] per token.  The C partial dot products of each token
+//     are exchanged through distributed shared memory, and two warps finish
+//     u and coef for the tile.
+//   * Second pass: the same boxes again (now from L2), while the first pass
+//     of the next tile and its exchange run ahead.  One thread issues
+//     tcgen05.mma:
+//       D1 = U' . PHI2^T  (M = 128 = 64 tokens x 2 streams, N = 64, K = 64):
+//         U' holds u in the first 32 K-columns of rows 0..63 and in the last
+//         32 of rows 64..127, PHI2 holds phi of stream 2p in its first 32
+//         K-columns and of stream 2p+1 in its last 32, so the two halves of
+//         D1 are (phi u) of the two streams;
+//       D2 += X^T . U     (M = 128 = 2 streams x 64 columns, read MN-major
+//         from the box, N = 32 (24 logits), K = 64 tokens): the dphi partial
+//         of the CTA's columns, resident in TMEM for the whole kernel.
+//     Eight epilogue warps (one token and stream per thread, as the TMEM
+//     lane layout gives) form the increment H_pre g_in + D1 + coef x in bf16
+//     over the x rows it came from, and one thread per stream pair adds that
+//     box to dx with a TMA reduction (the add happens in L2), so dx is never
+//     staged on chip.
+//   * phi (bf16, 24 logits padded to 32) stays in shared memory; u enters
+//     both products in bf16, far inside the tolerance of the bf16 dx and of
+//     the dphi sums.
+//   * Every wait is bounded (about one second); on expiry the kernel latches
+//     its device error word and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "launch.h"
+#include "mhc_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace mhc {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
+// This file's device error word (latched by bounded waits that ran out).
+__device__ unsigned g_bwd_fused_error;
+
+cudaError_t read_and_clear_bwd_fused_error(unsigned* word) {
+    cudaError_t e = cudaMemcpyFromSymbol(word, g_bwd_fused_error, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_bwd_fused_error, &zero, sizeof(unsigned));
+}
+
+namespace bwdfu {
+
+constexpr int TT = 64;                      // tokens per tile
+constexpr int KC = 64;                      // columns per chunk
+constexpr int MAX_NCK = 5;                  // chunks per stream per CTA
+constexpr int XSLOTS = 3;                   // ring of x / dx boxes
+constexpr int GSLOTS = 3;                   // ring of g_in boxes
+constexpr int SUB = TT * 128;               // one stream of a box: 64 tokens x 128 B
+constexpr int XBOX = 4 * SUB;               // 32 KB
+constexpr int GBOX = SUB;                   // 8 KB
+constexpr int PHI_BLK = KC * 128;           // 64 columns x [phi stream 2p | phi stream 2p+1]
+constexpr int NTHREADS = 512;               // 16 warps
+constexpr int DOT_WARP0 = 2, NDOT = 4;      // first-pass dot products
+constexpr int PREP_WARP0 = 6, NPREP = 2;    // cluster reduction, u and coef
+constexpr int EPI_WARP0 = 8, NEPI = 8;      // dx epilogue, then the dphi partial
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t D1_COL = 0;              // one 64-column buffer per stream pair
+constexpr uint32_t D2_COL = 128;            // (chunk, pair) -> 32 columns
+constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
+constexpr bool LOOKAHEAD = true;            // first pass of tile j+1 before the second of j
+
+// Ring discipline: a wait on an mbarrier phase parity is only sound for a
+// waiter at most one phase behind, so every consumer walks every position of
+// a ring in order -- it waits for each box to land and arrives on its EMPTY
+// barrier, also for the boxes it does not read.  x boxes: the MMA thread (a
+// commit where it read the box), the four dot warps and the eight epilogue
+// warps (in the second pass the leader of each stream pair arrives for its
+// four warps once the pair's dx reduction has read the box); g_in boxes: the
+// dot and the epilogue warps.
+constexpr uint32_t XEMPTY_COUNT = 1 + NDOT + NEPI;
+constexpr uint32_t GEMPTY_COUNT = NDOT + NEPI;
+
+enum : int {
+    BAR_XFULL = 0,
+    BAR_XEMPTY = BAR_XFULL + XSLOTS,
+    BAR_GFULL = BAR_XEMPTY + XSLOTS,
+    BAR_GEMPTY = BAR_GFULL + GSLOTS,
+    BAR_UFULL = BAR_GEMPTY + GSLOTS,
+    BAR_UEMPTY = BAR_UFULL + 1,
+    BAR_D1FULL = BAR_UEMPTY + 1,
+    BAR_D1EMPTY = BAR_D1FULL + 2,
+    BAR_D2DONE = BAR_D1EMPTY + 2,
+    BAR_PFULL = BAR_D2DONE + 1,             // partial dots of a tile parity, from every peer
+    BAR_PEMPTY = BAR_PFULL + 2,             // every peer has read them
+    NBARS = BAR_PEMPTY + 2
+};
+
+struct Layout {
+    static constexpr uint32_t XR = 0;
+    static constexpr uint32_t GR = XR + XSLOTS * XBOX;
+    static constexpr uint32_t PHI = GR + GSLOTS * GBOX;
+    static constexpr uint32_t UA = PHI + 2 * MAX_NCK * PHI_BLK;    // 128 rows x 128 B
+    static constexpr uint32_t U2 = UA + 128 * 128;                  // 32 rows x 128 B
+    static constexpr uint32_t SC = U2 + 32 * 128;                   // per token: H_pre[4], coef
+    static constexpr uint32_t PART = SC + TT * 32;                  // [2][TT] float4
+    static constexpr uint32_t BARS = PART + 2 * TT * 16;
+    static constexpr uint32_t MISC = BARS + NBARS * 8;
+    static constexpr uint32_t TOTAL = MISC + 64;
+};
+constexpr size_t SMEM_BYTES = Layout::TOTAL + 1024;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+static_assert(Layout::PHI % 1024 == 0 && Layout::UA % 1024 == 0 && Layout::U2 % 1024 == 0, "alignment");
+
+struct Params {
+    const float* phi;      // [K, 24]
+    const float* proj;     // [T, 24]
+    const float* alpha;    // [3]
+    float* rec;            // [T, REC]
+    __nv_bfloat16* dx;     // [T, 4, D]
+    float* part;           // [clusters, K, 24]
+    int64_t T;
+    int D;
+    int nck;               // chunks per stream per CTA
+    int ntiles;
+};
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         bool cluster_scope = false) {
+    auto test = [&] {
+        return cluster_scope ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+    };
+    if (test()) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (test()) return true;
+        if ((it & 63) == 0) {
+            if (*abort_flag) return false;
+            if (ptx::globaltimer() - t0 > WAIT_LIMIT_NS) {
+                atomicOr(&g_bwd_fused_error, 1u);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// Position in a ring of `n` slots: slot index and the parity of its use.
+struct Ring {
+    int slot = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void adv(int k, int n) {
+        slot += k;
+        while (slot >= n) {
+            slot -= n;
+            phase ^= 1u;
+        }
+    }
+};
+
+// Order of the passes: round r holds the first pass of tile p1(r) and then
+// the second pass of tile p2(r) (-1: none).  Every role walks the same
+// rounds, so that all agree on the ring positions.
+struct Sched {
+    int n;
+    __device__ int rounds() const { return LOOKAHEAD ? n + 1 : n; }
+    __device__ int p1(int r) const { return LOOKAHEAD ? (r < n ? r : -1) : r; }
+    __device__ int p2(int r) const { return LOOKAHEAD ? r - 1 : r; }
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+pre_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dx,
+                     const __grid_constant__ CUtensorMap tm_g, const Params p) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = ptx::smem_u32(smem);
+    auto bar = [&](int i) { return sbase + Layout::BARS + 8u * static_cast<uint32_t>(i); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Layout::MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Layout::MISC + 16);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    constexpr unsigned FULL = 0xffffffffu;
+    const uint32_t C = ptx::cluster_nctarank();
+    const uint32_t rank = ptx::cluster_ctarank();
+    const int cl = static_cast<int>(ptx::cluster_id_x());
+    const int ncl = static_cast<int>(ptx::nclusters_x());
+    const int nck = p.nck;
+    const int D = p.D;
+    const int64_t K = 4 * static_cast<int64_t>(D);
+    const int d0 = static_cast<int>(rank) * nck * KC;
+    const int ntl = p.ntiles > cl ? (p.ntiles - cl + ncl - 1) / ncl : 0;
+    const Sched sch{ntl};
+    auto tile_t0 = [&](int jl) { return static_cast<int64_t>(cl + jl * ncl) * TT; };
+
+    // ---- set-up ----------------------------------------------------------
+    if (tid == 0) {
+        for (int s = 0; s < XSLOTS; ++s) {
+            ptx::mbar_init(bar(BAR_XFULL + s), 1);
+            ptx::mbar_init(bar(BAR_XEMPTY + s), XEMPTY_COUNT);
+        }
+        for (int s = 0; s < GSLOTS; ++s) {
+            ptx::mbar_init(bar(BAR_GFULL + s), 1);
+            ptx::mbar_init(bar(BAR_GEMPTY + s), GEMPTY_COUNT);
+        }
+        ptx::mbar_init(bar(BAR_UFULL), NPREP * 32);
+        ptx::mbar_init(bar(BAR_UEMPTY), 1 + NEPI);
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(bar(BAR_D1FULL + b), 1);
+            ptx::mbar_init(bar(BAR_D1EMPTY + b), 4);
+            ptx::mbar_init(bar(BAR_PFULL + b), C);
+            ptx::mbar_init(bar(BAR_PEMPTY + b), C);
+        }
+        ptx::mbar_init(bar(BAR_D2DONE), 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&tm_x);
+        ptx::prefetch_tmap(&tm_dx);
+        ptx::prefetch_tmap(&tm_g);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    // PHI2 block (chunk c, pair pp): row r, K-columns 32a .. 32a+31 hold
+    // bf16(phi[(2pp + a) D + d0 + 64c + r, g]) for g < 24, zero for g >= 24.
+    for (int item = tid; item < nck * 1024; item += NTHREADS) {
+        const int q = item & 3, a = (item >> 2) & 1, r = (item >> 3) & 63, blk = item >> 9;
+        const int c = blk >> 1, pp = blk & 1;
+        const int64_t k = static_cast<int64_t>(2 * pp + a) * D + d0 + c * KC + r;
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int g0 = q * 8 + 2 * e;
+            const float v0 = g0 < NG ? p.phi[k * NG + g0] : 0.f;
+            const float v1 = g0 + 1 < NG ? p.phi[k * NG + g0 + 1] : 0.f;
+            w[e] = pack_bf16x2(v0, v1);
+        }
+        *reinterpret_cast<uint4*>(smem + Layout::PHI + blk * PHI_BLK + ptx::sw128_off(r, a * 32 + q * 8)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    // U' and U start zero; the preparation warps only ever write their u parts.
+    for (int i = tid; i < (128 * 128 + 32 * 128) / 16; i += NTHREADS)
+        reinterpret_cast<uint4*>(smem + Layout::UA)[i] = make_uint4(0u, 0u, 0u, 0u);
+    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    ptx::cluster_sync();   // peers' barriers are initialised before any remote arrive
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer ----
+        const uint64_t keep = ptx::policy_evict_last();    // first pass: read again soon
+        const uint64_t drop = ptx::policy_evict_first();   // second pass: last use
+        Ring X, G;
+        auto load_x = [&](const CUtensorMap* tm, int col, int64_t t0, uint64_t pol) -> bool {
+            bool ok = true;
+            if (lane == 0) ok = wait_bar(bar(BAR_XEMPTY + X.slot), X.phase ^ 1u, abort_flag);
+            if (!__shfl_sync(FULL, ok, 0)) return false;
+            if (lane == 0) {
+                const uint32_t fb = bar(BAR_XFULL + X.slot);
+                ptx::mbar_arrive_expect_tx(fb, XBOX);
+                ptx::tma_load_3d(sbase + Layout::XR + X.slot * XBOX, tm, col, static_cast<int>(t0), 0, fb, pol);
+            }
+            __syncwarp();
+            X.adv(1, XSLOTS);
+            return true;
+        };
+        auto load_g = [&](int col, int64_t t0, uint64_t pol) -> bool {
+            bool ok = true;
+            if (lane == 0) ok = wait_bar(bar(BAR_GEMPTY + G.slot), G.phase ^ 1u, abort_flag);
+            if (!__shfl_sync(FULL, ok, 0)) return false;
+            if (lane == 0) {
+                const uint32_t fb = bar(BAR_GFULL + G.slot);
+                ptx::mbar_arrive_expect_tx(fb, GBOX);
+                ptx::tma_load_2d(sbase + Layout::GR + G.slot * GBOX, &tm_g, col, static_cast<int>(t0), fb, pol);
+            }
+            __syncwarp();
+            G.adv(1, GSLOTS);
+            return true;
+        };
+        for (int r = 0; r < sch.rounds(); ++r) {
+            const int a = sch.p1(r), b = sch.p2(r);
+            if (a >= 0) {
+                const int64_t t0 = tile_t0(a);
+                for (int c = 0; c < nck; ++c)
+                    if (!load_x(&tm_x, d0 + c * KC, t0, keep) || !load_g(d0 + c * KC, t0, keep)) goto done;
+            }
+            if (b >= 0) {
+                const int64_t t0 = tile_t0(b);
+                for (int c = 0; c < nck; ++c)
+                    if (!load_x(&tm_x, d0 + c * KC, t0, drop) || !load_g(d0 + c * KC, t0, drop)) goto done;
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------- MMA issuer -----
+        constexpr uint32_t IDESC1 = ptx::idesc_bf16_f32(128, KC);               // D1: both K-major
+        constexpr uint32_t IDESC2 = ptx::idesc_bf16_f32(128, 32) | (1u << 15);  // D2: A (x^T) MN-major
+        Ring X;
+        int s = 0, ju = 0;
+        // a box this thread does not read: wait for it, then release it
+        auto pass_x = [&]() -> bool {
+            bool ok = true;
+            if (lane == 0) {
+                ok = wait_bar(bar(BAR_XFULL + X.slot), X.phase, abort_flag);
+                if (ok) ptx::mbar_arrive(bar(BAR_XEMPTY + X.slot));
+            }
+            X.adv(1, XSLOTS);
+            return __shfl_sync(FULL, ok, 0);
+        };
+        for (int r = 0; r < sch.rounds(); ++r) {
+            if (sch.p1(r) >= 0)
+                for (int c = 0; c < nck; ++c)
+                    if (!pass_x()) goto done;
+            if (sch.p2(r) < 0) continue;
+            bool ok = true;
+            if (lane == 0) ok = wait_bar(bar(BAR_UFULL), ju & 1, abort_flag);
+            if (!__shfl_sync(FULL, ok, 0)) goto done;
+            for (int c = 0; c < nck; ++c, ++s) {
+                if (lane == 0) ok = wait_bar(bar(BAR_XFULL + X.slot), X.phase, abort_flag);
+                if (!__shfl_sync(FULL, ok, 0)) goto done;
+                const uint32_t xs = sbase + Layout::XR + X.slot * XBOX;
+                for (int pp = 0; pp < 2; ++pp) {
+                    if (lane == 0) ok = wait_bar(bar(BAR_D1EMPTY + pp), (s & 1) ^ 1, abort_flag);
+                    if (!__shfl_sync(FULL, ok, 0)) goto done;
+                    ptx::tc_fence_after();
+                    if (lane == 0) {
+                        // D2 first: the commit of D1FULL then also tells the pair's
+                        // epilogue that the MMA no longer reads its x sub-boxes,
+                        // which it overwrites with the dx increment
+#pragma unroll
+                        for (int kk = 0; kk < TT / 16; ++kk)
+                            ptx::tc_mma_f16(tmem + D2_COL + (c * 2 + pp) * 32,
+                                            ptx::sw128_mnmajor_desc(xs + pp * 2 * SUB + kk * 2048, SUB, 1024),
+                                            ptx::sw128_kmajor_desc(sbase + Layout::U2 + kk * 32), IDESC2,
+                                            (ju | kk) != 0);
+                        const uint32_t phi = sbase + Layout::PHI + (c * 2 + pp) * PHI_BLK;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            ptx::tc_mma_f16(tmem + D1_COL + pp * KC,
+                                            ptx::sw128_kmajor_desc(sbase + Layout::UA + kk * 32),
+                                            ptx::sw128_kmajor_desc(phi + kk * 32), IDESC1, kk != 0);
+                        ptx::tc_commit(bar(BAR_D1FULL + pp));
+                    }
+                    __syncwarp();
+                }
+                if (lane == 0) ptx::tc_commit(bar(BAR_XEMPTY + X.slot));
+                __syncwarp();
+                X.adv(1, XSLOTS);
+            }
+            if (lane == 0) ptx::tc_commit(bar(BAR_UEMPTY));
+            __syncwarp();
+            ++ju;
+        }
+        if (lane == 0) ptx::tc_commit(bar(BAR_D2DONE));
+        __syncwarp();
+    } else if (warp < PREP_WARP0) {
+        // -------------------------------------- first pass: dot products --
+        const int q = tid - DOT_WARP0 * 32;            // 0..127
+        const int t = q >> 1, h = q & 1;               // token, half of each chunk
+        Ring X, G;
+        int jd = 0;
+        for (int r = 0; r < sch.rounds(); ++r) {
+            if (sch.p1(r) >= 0) {
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                bool ok = true;
+                for (int c = 0; c < nck && ok; ++c) {
+                    ok = __all_sync(FULL, wait_bar(bar(BAR_XFULL + X.slot), X.phase, abort_flag)) &&
+                         __all_sync(FULL, wait_bar(bar(BAR_GFULL + G.slot), G.phase, abort_flag));
+                    if (!ok) break;
+                    const unsigned char* xb = smem + Layout::XR + X.slot * XBOX;
+                    const unsigned char* gb = smem + Layout::GR + G.slot * GBOX;
+#pragma unroll
+                    for (int cq = 0; cq < 4; ++cq) {
+                        const uint32_t off = static_cast<uint32_t>(t * 128 + (((h * 4 + cq) ^ (t & 7)) << 4));
+                        float fg[8];
+                        Vec<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(gb + off), fg);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            float fx[8];
+                            Vec<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(xb + i * SUB + off), fx);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc[i] = fmaf(fg[e], fx[e], acc[i]);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::mbar_arrive(bar(BAR_XEMPTY + X.slot));
+                        ptx::mbar_arrive(bar(BAR_GEMPTY + G.slot));
+                    }
+                    X.adv(1, XSLOTS);
+                    G.adv(1, GSLOTS);
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[i] += __shfl_xor_sync(FULL, acc[i], 1);
+                const int ps = jd & 1;
+                if (ok) ok = __all_sync(FULL, wait_bar(bar(BAR_PEMPTY + ps), ((jd >> 1) & 1) ^ 1, abort_flag, true));
+                if (ok && h == 0)
+                    reinterpret_cast<float4*>(smem + Layout::PART + ps * TT * 16)[t] =
+                        make_float4(acc[0], acc[1], acc[2], acc[3]);
+                if (ptx::named_bar_or(1, NDOT * 32, !ok)) goto done;
+                if (warp == DOT_WARP0 && lane < static_cast<int>(C)) {
+                    ptx::fence_acq_rel_cluster();
+                    ptx::mbar_arrive_remote(ptx::mapa(bar(BAR_PFULL + ps), static_cast<uint32_t>(lane)));
+                }
+                ++jd;
+            }
+            if (sch.p2(r) >= 0) {
+                // second-pass boxes (x, g_in per chunk): wait, release
+                bool ok = true;
+                for (int c = 0; c < nck && ok; ++c) {
+                    ok = __all_sync(FULL, wait_bar(bar(BAR_XFULL + X.slot), X.phase, abort_flag));
+                    if (ok && lane == 0) ptx::mbar_arrive(bar(BAR_XEMPTY + X.slot));
+                    X.adv(1, XSLOTS);
+                    if (!ok) break;
+                    ok = __all_sync(FULL, wait_bar(bar(BAR_GFULL + G.slot), G.phase, abort_flag));
+                    if (ok && lane == 0) ptx::mbar_arrive(bar(BAR_GEMPTY + G.slot));
+                    G.adv(1, GSLOTS);
+                }
+                if (ptx::named_bar_or(1, NDOT * 32, !ok)) goto done;
+            }
+        }
+    } else if (warp < EPI_WARP0) {
+        // ------------------------------ cluster reduction, u and coef -----
+        const int t = tid - PREP_WARP0 * 32;           // 0..63: token of the tile
+        const float apre = p.alpha[0];
+        const float invK = 1.0f / static_cast<float>(K);
+        for (int jl = 0; jl < ntl; ++jl) {
+            const int64_t tg = tile_t0(jl) + t;
+            const bool valid = tg < p.T;
+            float u[32], hp[4] = {0.f, 0.f, 0.f, 0.f}, ds[4] = {0.f, 0.f, 0.f, 0.f};
+            float pj[4] = {0.f, 0.f, 0.f, 0.f}, coef_rest = 0.f, s = 0.f;
+#pragma unroll
+            for (int g = 0; g < 32; ++g) u[g] = 0.f;
+            if (valid) {
+                const float* rr = p.rec + tg * REC;
+#pragma unroll
+                for (int v = 1; v < 6; ++v) {
+                    const float4 a = reinterpret_cast<const float4*>(rr + REC_U)[v];
+                    u[4 * v] = a.x; u[4 * v + 1] = a.y; u[4 * v + 2] = a.z; u[4 * v + 3] = a.w;
+                }
+                const float4 a = reinterpret_cast<const float4*>(rr + REC_HPRE)[0];
+                hp[0] = a.x; hp[1] = a.y; hp[2] = a.z; hp[3] = a.w;
+                const float4 cs = reinterpret_cast<const float4*>(rr + REC_COEF)[0];
+                coef_rest = cs.x;
+                s = cs.y;
+                const float4 dd = reinterpret_cast<const float4*>(rr + REC_DSIG)[0];
+                ds[0] = dd.x; ds[1] = dd.y; ds[2] = dd.z; ds[3] = dd.w;
+                const float4 pq = reinterpret_cast<const float4*>(p.proj + tg * NG)[0];
+                pj[0] = pq.x; pj[1] = pq.y; pj[2] = pq.z; pj[3] = pq.w;
+            }
+            const int ps = jl & 1;
+            bool ok = __all_sync(FULL, wait_bar(bar(BAR_PFULL + ps), (jl >> 1) & 1, abort_flag, true));
+            float dh[4] = {0.f, 0.f, 0.f, 0.f};
+            if (ok) {
+                const uint32_t src = sbase + Layout::PART + ps * TT * 16 + t * 16;
+#pragma unroll 4
+                for (uint32_t pr = 0; pr < C; ++pr) {
+                    const float4 v = ptx::ld_cluster_v4(ptx::mapa(src, pr));
+                    dh[0] += v.x; dh[1] += v.y; dh[2] += v.z; dh[3] += v.w;
+                }
+            }
+            if (ptx::named_bar_or(2, NPREP * 32, !ok)) goto done;
+            if (t < static_cast<int>(C)) {
+                ptx::fence_acq_rel_cluster();
+                ptx::mbar_arrive_remote(ptx::mapa(bar(BAR_PEMPTY + ps), static_cast<uint32_t>(t)));
+            }
+            float dl[4], cadd = 0.f, da0 = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                dl[i] = dh[i] * ds[i];
+                u[i] = s * apre * dl[i];
+                cadd = fmaf(u[i], pj[i], cadd);
+                da0 = fmaf(dl[i], pj[i], da0);
+            }
+            const float coef = coef_rest - s * cadd * invK;
+            if (valid && rank == 0) {
+                reinterpret_cast<float4*>(p.rec + tg * REC + REC_DL)[0] = make_float4(dl[0], dl[1], dl[2], dl[3]);
+                p.rec[tg * REC + REC_DA] = da0;
+            }
+            if (!__all_sync(FULL, wait_bar(bar(BAR_UEMPTY), (jl & 1) ^ 1, abort_flag))) goto done;
+            // U' rows t and 64 + t; U column t (rows g < 24); per-token scalars
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+                const uint4 w = make_uint4(pack_bf16x2(u[8 * qq], u[8 * qq + 1]), pack_bf16x2(u[8 * qq + 2], u[8 * qq + 3]),
+                                           pack_bf16x2(u[8 * qq + 4], u[8 * qq + 5]),
+                                           pack_bf16x2(u[8 * qq + 6], u[8 * qq + 7]));
+                *reinterpret_cast<uint4*>(smem + Layout::UA + ptx::sw128_off(t, qq * 8)) = w;
+                *reinterpret_cast<uint4*>(smem + Layout::UA + ptx::sw128_off(64 + t, 32 + qq * 8)) = w;
+            }
+#pragma unroll
+            for (int g = 0; g < NG; ++g)
+                *reinterpret_cast<__nv_bfloat16*>(smem + Layout::U2 + ptx::sw128_off(g, t)) = __float2bfloat16_rn(u[g]);
+            float* sc = reinterpret_cast<float*>(smem + Layout::SC) + t * 8;
+            reinterpret_cast<float4*>(sc)[0] = make_float4(hp[0], hp[1], hp[2], hp[3]);
+            sc[4] = coef;
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(bar(BAR_UFULL));
+        }
+    } else {
+        // ------------------------------------------------- epilogue -------
+        const int e = tid - EPI_WARP0 * 32;            // 0..255
+        const int pp = e >> 7;                         // stream pair
+        const int q = e & 127;                         // TMEM lane = row of D1 / D2
+        const int t = q & 63;                          // token of the tile
+        const int si = 2 * pp + (q >> 6);              // stream
+        const int wq = warp & 3;                       // TMEM lane quarter of this warp
+        const bool leader = q == 0;                    // issues the pair's dx reductions
+        Ring X, G;
+        int s = 0, ju = 0, pend = -1;                  // pend: x slot whose reduction may still read it
+        bool aborted = false;
+        // release the slot of the last reduction once the TMA has read it
+        auto flush = [&] {
+            if (leader && pend >= 0) {
+                ptx::bulk_wait_read<0>();
+                ptx::mbar_arrive_cnt(bar(BAR_XEMPTY + pend), 4);
+                pend = -1;
+            }
+        };
+        for (int r = 0; r < sch.rounds() && !aborted; ++r) {
+            if (sch.p1(r) >= 0) {
+                // first-pass boxes (x, g_in per chunk): wait, release
+                flush();
+                for (int c = 0; c < nck && !aborted; ++c) {
+                    if (!__all_sync(FULL, wait_bar(bar(BAR_XFULL + X.slot), X.phase, abort_flag)) ||
+                        !__all_sync(FULL, wait_bar(bar(BAR_GFULL + G.slot), G.phase, abort_flag))) {
+                        aborted = true;
+                        break;
+                    }
+                    if (lane == 0) {
+                        ptx::mbar_arrive(bar(BAR_XEMPTY + X.slot));
+                        ptx::mbar_arrive(bar(BAR_GEMPTY + G.slot));
+                    }
+                    X.adv(1, XSLOTS);
+                    G.adv(1, GSLOTS);
+                }
+                if (aborted) break;
+            }
+            const int b = sch.p2(r);
+            if (b < 0) continue;
+            const int t0 = static_cast<int>(tile_t0(b));
+            // every thread of the pair passes the same named barriers, so a
+            // failed wait is carried in `ok` and acted on at the barrier
+            bool ok = __all_sync(FULL, wait_bar(bar(BAR_UFULL), ju & 1, abort_flag));
+            float hpre = 0.f, cf = 0.f;
+            if (ok) {
+                const float* sc = reinterpret_cast<const float*>(smem + Layout::SC) + t * 8;
+                hpre = sc[si];
+                cf = sc[4];
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(BAR_UEMPTY));
+            }
+            for (int c = 0; c < nck; ++c, ++s) {
+                ok = ok && __all_sync(FULL, wait_bar(bar(BAR_D1FULL + pp), s & 1, abort_flag)) &&
+                     __all_sync(FULL, wait_bar(bar(BAR_XFULL + X.slot), X.phase, abort_flag)) &&
+                     __all_sync(FULL, wait_bar(bar(BAR_GFULL + G.slot), G.phase, abort_flag));
+                unsigned char* xb = smem + Layout::XR + X.slot * XBOX + si * SUB;
+                if (ok) {
+                    ptx::tc_fence_after();
+                    uint32_t v[4][16];
+                    const uint32_t ta = tmem + (static_cast<uint32_t>(wq * 32) << 16) + D1_COL + pp * KC;
+#pragma unroll
+                    for (int h16 = 0; h16 < 4; ++h16) ptx::tmem_ld16(ta + h16 * 16, v[h16]);
+                    ptx::tmem_wait_ld();
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(bar(BAR_D1EMPTY + pp));
+                    const unsigned char* gb = smem + Layout::GR + G.slot * GBOX;
+                    // dx increment of this token and stream, written over the
+                    // x row it was computed from (same swizzled place)
+#pragma unroll
+                    for (int cq = 0; cq < 8; ++cq) {
+                        const uint32_t off = static_cast<uint32_t>(t * 128 + ((cq ^ (t & 7)) << 4));
+                        float fx[8], fg[8], o[8];
+                        Vec<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(xb + off), fx);
+                        Vec<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(gb + off), fg);
+#pragma unroll
+                        for (int el = 0; el < 8; ++el) {
+                            const int col = cq * 8 + el;
+                            o[el] = fmaf(hpre, fg[el], fmaf(cf, fx[el], __uint_as_float(v[col >> 4][col & 15])));
+                        }
+                        *reinterpret_cast<uint4*>(xb + off) = Vec<__nv_bfloat16>::pack(o);
+                    }
+                    ptx::fence_proxy_async_smem();
+                }
+                if (ptx::named_bar_or(3 + pp, 128, !ok)) {
+                    aborted = true;
+                    break;
+                }
+                if (leader) {
+                    // dx[t0.., 2pp..2pp+1, d0 + 64c ..] += the pair's two sub-boxes
+                    ptx::tma_reduce_add_3d(&tm_dx, d0 + c * KC, t0, 2 * pp,
+                                           sbase + Layout::XR + X.slot * XBOX + pp * 2 * SUB);
+                    ptx::bulk_commit();
+                    ptx::mbar_arrive_cnt(bar(BAR_GEMPTY + G.slot), 4);
+                    if (pend >= 0) {
+                        ptx::bulk_wait_read<1>();
+                        ptx::mbar_arrive_cnt(bar(BAR_XEMPTY + pend), 4);
+                    }
+                    pend = X.slot;
+                }
+                X.adv(1, XSLOTS);
+                G.adv(1, GSLOTS);
+            }
+            ++ju;
+        }
+        flush();
+        if (leader) ptx::bulk_wait<0>();   // the reductions are complete before the kernel ends
+        // dphi partial of this cluster: D2 row q of (chunk c, pair pp) is
+        // column k = si * D + d0 + 64c + t.
+        if (!aborted && __all_sync(FULL, wait_bar(bar(BAR_D2DONE), 0, abort_flag))) {
+            ptx::tc_fence_after();
+            float* out = p.part + static_cast<int64_t>(cl) * K * NG;
+            for (int c = 0; c < nck; ++c) {
+                uint32_t w0[16], w1[16];
+                const uint32_t ta = tmem + (static_cast<uint32_t>(wq * 32) << 16) + D2_COL + (c * 2 + pp) * 32;
+                ptx::tmem_ld16(ta, w0);
+                ptx::tmem_ld16(ta + 16, w1);
+                ptx::tmem_wait_ld();
+                float4* o4 = reinterpret_cast<float4*>(out + (static_cast<int64_t>(si) * D + d0 + c * KC + t) * NG);
+                const bool any = ju > 0;
+#pragma unroll
+                for (int v4 = 0; v4 < 4; ++v4)
+                    o4[v4] = any ? make_float4(__uint_as_float(w0[4 * v4]), __uint_as_float(w0[4 * v4 + 1]),
+                                               __uint_as_float(w0[4 * v4 + 2]), __uint_as_float(w0[4 * v4 + 3]))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int v4 = 0; v4 < 2; ++v4)
+                    o4[4 + v4] = any ? make_float4(__uint_as_float(w1[4 * v4]), __uint_as_float(w1[4 * v4 + 1]),
+                                                   __uint_as_float(w1[4 * v4 + 2]), __uint_as_float(w1[4 * v4 + 3]))
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+    }
+done:
+    __syncthreads();
+    if (*abort_flag) {
+        // let copies already issued land before the shared memory goes away
+        const uint64_t t0 = ptx::globaltimer();
+        while (ptx::globaltimer() - t0 < 20000ull) {
+        }
+    }
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, TMEM_COLS);
+    }
+    ptx::cluster_sync();   // no CTA leaves while a peer may still touch its shared memory
+}
+
+// Smallest cluster whose per-CTA column slice is a whole number of 64-column
+// chunks, at most MAX_NCK of them (phi slice and dphi accumulators on chip).
+int cluster_for(int64_t D) {
+    if (D <= 0 || D % KC != 0) return 0;
+    const int64_t nc = D / KC;
+    for (int C : {1, 2, 4, 8, 16})
+        if (nc % C == 0 && nc / C <= MAX_NCK) return C;
+    return 0;
+}
+
+bool set_attributes_once() {
+    static int ok = -1;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        ok = cudaFuncSetAttribute(pre_bwd_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(SMEM_BYTES)) == cudaSuccess &&
+             cudaFuncSetAttribute(pre_bwd_fused_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                 cudaSuccess;
+    });
+    return ok == 1;
+}
+
+cudaLaunchConfig_t config(int C, int nclusters, cudaStream_t s, cudaLaunchAttribute* attr) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(nclusters * C));
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(C);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+// Clusters of size C that fit on the device at once (per device, cached).
+int max_clusters(int C) {
+    static int cache[64][5];
+    static std::once_flag once[64][5];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int ci = 0;
+    while ((1 << ci) < C) ++ci;
+    if (ci > 4 || (1 << ci) != C) return 0;
+    std::call_once(once[dev][ci], [&] {
+        int n = 0;
+        cudaLaunchAttribute attr[1];
+        cudaLaunchConfig_t cfg = config(C, 152 / C > 0 ? 152 / C : 1, nullptr, attr);
+        if (!set_attributes_once() || cudaOccupancyMaxActiveClusters(&n, pre_bwd_fused_kernel, &cfg) != cudaSuccess)
+            n = 0;
+        cache[dev][ci] = n;
+    });
+    return cache[dev][ci];
+}
+
+// dims (d, t, stream) of a [T, 4, D] tensor: box = 64 columns x 64 tokens x
+// `streams` streams, laid out in shared memory as [stream][token][64 columns]
+bool encode_x(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* tm, const void* base, int64_t T, int64_t D,
+              int streams) {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(T), 4};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(8 * D), static_cast<cuuint64_t>(2 * D)};
+    const cuuint32_t box[3] = {KC, TT, static_cast<cuuint32_t>(streams)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_g(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* tm, const void* base, int64_t T, int64_t D) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(T)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(2 * D)};
+    const cuuint32_t box[2] = {KC, TT};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace bwdfu
+
+bool pre_bwd_fused_supports(int64_t T, int64_t D) {
+    if (T < bwdfu::TT || T >= (int64_t(1) << 31) || 4 * D * T >= (int64_t(1) << 46)) return false;
+    const int C = bwdfu::cluster_for(D);
+    return C > 0 && tensor_map_encoder() != nullptr && bwdfu::max_clusters(C) > 0;
+}
+
+cudaError_t launch_pre_bwd_fused_main(const void* g_in, const void* x, const float* phi,
+                                      const float* proj, const float* alpha, float* rec,
+                                      int64_t T, int64_t D, int64_t max_parts, void* dx,
+                                      float* part, int64_t* nparts, cudaStream_t s) {
+    auto encode = tensor_map_encoder();
+    const int C = bwdfu::cluster_for(D);
+    if (encode == nullptr || C == 0 || !bwdfu::set_attributes_once()) return cudaErrorNotSupported;
+    CUtensorMap tx, tdx, tg;
+    // x is read as 4-stream boxes; dx only receives reductions of 2-stream boxes
+    if (!bwdfu::encode_x(encode, &tx, x, T, D, 4) || !bwdfu::encode_x(encode, &tdx, dx, T, D, 2) ||
+        !bwdfu::encode_g(encode, &tg, g_in, T, D))
+        return cudaErrorInvalidValue;
+    bwdfu::Params prm;
+    prm.phi = phi;
+    prm.proj = proj;
+    prm.alpha = alpha;
+    prm.rec = rec;
+    prm.dx = static_cast<__nv_bfloat16*>(dx);
+    prm.part = part;
+    prm.T = T;
+    prm.D = static_cast<int>(D);
+    prm.nck = static_cast<int>(D / bwdfu::KC / C);
+    prm.ntiles = static_cast<int>((T + bwdfu::TT - 1) / bwdfu::TT);
+    int64_t ncl = bwdfu::max_clusters(C);
+    if (ncl > prm.ntiles) ncl = prm.ntiles;
+    if (ncl > max_parts) ncl = max_parts;
+    if (ncl <= 0) return cudaErrorNotSupported;
+    *nparts = ncl;
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = bwdfu::config(C, static_cast<int>(ncl), s, attr);
+    return cudaLaunchKernelEx(&cfg, bwdfu::pre_bwd_fused_kernel, tx, tdx, tg, prm);
+}
+
+}  // namespace mhc

@@ -117,24 +117,8 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     }
 }
 
-// Descriptor of an MN-major operand in the 128-byte swizzle: 64 contiguous
-// elements per 128-byte row, 8-row groups `sbo` apart along K, consecutive
-// 64-element blocks along M/N `lbo` apart.
-__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
-    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
-    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
-    d |= static_cast<uint64_t>(1) << 46;
-    d |= static_cast<uint64_t>(2) << 61;
-    return d;
-}
-
-// Byte offset of element (row, col) in a 128-byte-swizzled tile whose rows
-// are 128 bytes (64 bf16) long.
-__device__ __forceinline__ uint32_t sw128_off(int row, int col) {
-    return static_cast<uint32_t>(row * 128 + (((col >> 3) ^ (row & 7)) << 4) + (col & 7) * 2);
-}
+using ptx::sw128_mnmajor_desc;
+using ptx::sw128_off;
 
 __global__ void __launch_bounds__(NTHREADS, 1)
 pre_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dx,

@@ -42,7 +42,8 @@ namespace mhc {
 // mhc_get_last_device_error().
 __device__ unsigned g_device_error;
 
-cudaError_t read_and_clear_bwd_tc_error(unsigned* word);   // pre_bwd_tc.cu
+cudaError_t read_and_clear_bwd_tc_error(unsigned* word);      // pre_bwd_tc.cu
+cudaError_t read_and_clear_bwd_fused_error(unsigned* word);   // pre_bwd_fused.cu
 
 cudaError_t read_and_clear_device_error(unsigned* word, cudaStream_t s) {
     cudaError_t e = cudaStreamSynchronize(s);
@@ -54,6 +55,10 @@ cudaError_t read_and_clear_device_error(unsigned* word, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     unsigned other = 0;
     e = read_and_clear_bwd_tc_error(&other);
+    if (e != cudaSuccess) return e;
+    *word |= other;
+    other = 0;
+    e = read_and_clear_bwd_fused_error(&other);
     *word |= other;
     return e;
 }

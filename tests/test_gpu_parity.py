@@ -62,6 +62,9 @@ def test_workload4_bf16_fwd_bwd_s4096():
 @pytest.mark.parametrize("T,D,dtype", [
     (1, 5120, "bf16"), (3, 8, "bf16"), (65, 40, "bf16"), (130, 264, "bf16"),
     (200, 1024, "bf16"), (333, 2560, "bf16"), (129, 5120, "bf16"),
+    # widths that give clusters of 1 and 16 with 4, 5 and 3 chunks per CTA,
+    # and one (6144) that the one-pass backward does not take
+    (64, 256, "bf16"), (150, 320, "bf16"), (100, 3072, "bf16"), (160, 6144, "bf16"),
     (1, 4, "f32"), (67, 12, "f32"), (130, 260, "f32"),
 ])
 def test_ragged_shapes_fwd_bwd(T, D, dtype):
