@@ -3,15 +3,21 @@
 // post backward (one warp per token):
 //   dx[j] = sum_i H_res[i,j] g[i],  dy = sum_i H_post[i] g[i],
 //   dH_post[i] = <g[i], y>,         dH_res[i,j] = <g[i], x[j]>
-// pre backward, four launches:
+// pre backward, bf16 widths the cluster kernel tiles (pre_bwd_fused.cu):
+//   1. token  (thread per token): gate derivatives, Sinkhorn VJP from the
+//      recomputed forward, the post / residual parts of u = inv_rms *
+//      alpha_grp * dlogits and their share of the RMSNorm coefficient of x,
+//      written to a per-token record (none of it needs dH_pre)
+//   2. one-pass cluster kernel: dH_pre, the pre-gate parts, dx, dphi partials
+//   3. reduce : dphi over partials, db and dalpha over tokens (fixed order,
+//      no atomics)
+// otherwise (float32, other widths) five launches:
 //   1. dots   (warp per token): dH_pre[i] = <g_in, x[i]>
-//   2. token  (thread per token): gate derivatives, Sinkhorn VJP from the
-//      recomputed forward, u = inv_rms * alpha_grp * dlogits and the RMSNorm
-//      coefficient of x, written to a per-token record
-//   3. main   (K slice x token block): dx += H_pre[i] g_in + phi u + coef x,
-//      and the block's partial dphi = sum_t x_t u_t^T
-//   4. reduce : dphi over token blocks, db and dalpha over tokens (fixed
-//      order, no atomics)
+//   2. token  as above, now with dH_pre
+//   3. main   (K slice x token block, tensor cores for bf16 widths that are
+//      a multiple of 256): dx += H_pre[i] g_in + phi u + coef x, and the
+//      block's partial dphi = sum_t x_t u_t^T
+//   4. reduce : as above
 // Derivation (with s = inv_rms, v = alpha_grp * dlogits, proj = s * x.phi):
 //   dx_norm = s * phi v - s^2 * x * (v . proj) / K,   dphi = sum_t s_t x_t v_t^T
 // Layer definition: "openPangu 2.0 -- architecture, training and Ascend
@@ -188,7 +194,6 @@ pre_bwd_token_kernel(const float* __restrict__ dH_post, const float* __restrict_
 //    dphi of a token block.  Each thread owns two consecutive k.
 constexpr int MB_THREADS = 128;
 constexpr int MB_KS = 2 * MB_THREADS;   // K elements per CTA
-constexpr int MB_TCH = 32;              // tokens staged per chunk
 
 // Two consecutive activations of one token, kept in their storage form
 // (one 32-bit word for bf16, two floats for float32) until they are used.
