@@ -323,6 +323,11 @@ pre_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
         // ------------------------------------------------- MMA issuer -----
         constexpr uint32_t IDESC1 = ptx::idesc_bf16_f32(128, KC);               // D1: both K-major
         constexpr uint32_t IDESC2 = ptx::idesc_bf16_f32(128, 32) | (1u << 15);  // D2: A (x^T) MN-major
+        // descriptors built once; the loop only moves their start address
+        const uint64_t desc_x0 = ptx::sw128_mnmajor_desc(sbase + Layout::XR, SUB, 1024);
+        const uint64_t desc_u2 = ptx::sw128_kmajor_desc(sbase + Layout::U2);
+        const uint64_t desc_ua = ptx::sw128_kmajor_desc(sbase + Layout::UA);
+        const uint64_t desc_phi = ptx::sw128_kmajor_desc(sbase + Layout::PHI);
         Ring X;
         int s = 0, ju = 0;
         // a box this thread does not read: wait for it, then release it
@@ -346,7 +351,6 @@ pre_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
             for (int c = 0; c < nck; ++c, ++s) {
                 if (lane == 0) ok = wait_bar(bar(BAR_XFULL + X.slot), X.phase, abort_flag);
                 if (!__shfl_sync(FULL, ok, 0)) goto done;
-                const uint32_t xs = sbase + Layout::XR + X.slot * XBOX;
                 for (int pp = 0; pp < 2; ++pp) {
                     if (lane == 0) ok = wait_bar(bar(BAR_D1EMPTY + pp), (s & 1) ^ 1, abort_flag);
                     if (!__shfl_sync(FULL, ok, 0)) goto done;
@@ -355,18 +359,16 @@ pre_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
                         // D2 first: the commit of D1FULL then also tells the pair's
                         // epilogue that the MMA no longer reads its x sub-boxes,
                         // which it overwrites with the dx increment
+                        const uint64_t dx2 = ptx::desc_add(desc_x0, X.slot * XBOX + pp * 2 * SUB);
 #pragma unroll
                         for (int kk = 0; kk < TT / 16; ++kk)
-                            ptx::tc_mma_f16(tmem + D2_COL + (c * 2 + pp) * 32,
-                                            ptx::sw128_mnmajor_desc(xs + pp * 2 * SUB + kk * 2048, SUB, 1024),
-                                            ptx::sw128_kmajor_desc(sbase + Layout::U2 + kk * 32), IDESC2,
-                                            (ju | kk) != 0);
-                        const uint32_t phi = sbase + Layout::PHI + (c * 2 + pp) * PHI_BLK;
+                            ptx::tc_mma_f16(tmem + D2_COL + (c * 2 + pp) * 32, ptx::desc_add(dx2, kk * 2048),
+                                            ptx::desc_add(desc_u2, kk * 32), IDESC2, (ju | kk) != 0);
+                        const uint64_t dphi = ptx::desc_add(desc_phi, (c * 2 + pp) * PHI_BLK);
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            ptx::tc_mma_f16(tmem + D1_COL + pp * KC,
-                                            ptx::sw128_kmajor_desc(sbase + Layout::UA + kk * 32),
-                                            ptx::sw128_kmajor_desc(phi + kk * 32), IDESC1, kk != 0);
+                            ptx::tc_mma_f16(tmem + D1_COL + pp * KC, ptx::desc_add(desc_ua, kk * 32),
+                                            ptx::desc_add(dphi, kk * 32), IDESC1, kk != 0);
                         ptx::tc_commit(bar(BAR_D1FULL + pp));
                     }
                     __syncwarp();

@@ -217,6 +217,11 @@ pre_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
         // ------------------------------------------------- MMA issuer -----
         constexpr uint32_t IDESC1 = ptx::idesc_bf16_f32(TT, KC) | (1u << 15);    // A (U) MN-major
         constexpr uint32_t IDESC2 = ptx::idesc_bf16_f32(128, KC) | (1u << 16);   // B (X) MN-major
+        // descriptors built once; the loop only moves their start address
+        const uint64_t desc_aphi0 = ptx::sw128_kmajor_desc(sbase + Layout::APHI);
+        const uint64_t desc_x0 = sw128_mnmajor_desc(sbase + Layout::STAGE, ARR_BYTES, 1024);
+        const uint64_t desc_u2mn0 = sw128_mnmajor_desc(sbase + Layout::UBUF, U2_ATOM, 1024);
+        const uint64_t desc_u2k0 = ptx::sw128_kmajor_desc(sbase + Layout::UBUF);
         int stage = 0;
         uint32_t round = 0;
         int q = 0;
@@ -225,7 +230,6 @@ pre_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
             bool ok = true;
             if (lane == 0) ok = wait_bar(bar(BAR_UFULL + ub), (j >> 1) & 1, abort_flag);
             if (!__shfl_sync(FULL, ok, 0)) goto done;
-            const uint32_t u2 = sbase + Layout::UBUF + ub * UBUF_BYTES;
             for (int c = 0; c < NCH; ++c, ++q) {
                 const int db = q & 1;
                 if (lane == 0) ok = wait_bar(bar(BAR_D1EMPTY + db), ((q >> 1) & 1) ^ 1, abort_flag);
@@ -234,21 +238,22 @@ pre_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
                 if (!__shfl_sync(FULL, ok, 0)) goto done;
                 ptx::tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t aphi = sbase + Layout::APHI + c * APHI_CHUNK;
-                    const uint32_t xs = sbase + Layout::STAGE + stage * STAGE_BYTES;
+                    const uint64_t aphi = ptx::desc_add(desc_aphi0, c * APHI_CHUNK);
+                    const uint64_t xs = ptx::desc_add(desc_x0, stage * STAGE_BYTES);
+                    const uint32_t u2o = ub * UBUF_BYTES;
                     // D1 = U . A_phi^T: A = U2T read MN-major (tokens contiguous,
                     // 64-token atoms U2_ATOM apart), K = 32 logit rows
 #pragma unroll
                     for (int kk = 0; kk < 2; ++kk)
-                        ptx::tc_mma_f16(tmem + D1_COL + db * KC, sw128_mnmajor_desc(u2 + kk * 2048, U2_ATOM, 1024),
-                                        ptx::sw128_kmajor_desc(aphi + kk * 32), IDESC1, kk != 0);
+                        ptx::tc_mma_f16(tmem + D1_COL + db * KC, ptx::desc_add(desc_u2mn0, u2o + kk * 2048),
+                                        ptx::desc_add(aphi, kk * 32), IDESC1, kk != 0);
                     // D2T += U2T . X: A = U2T K-major (rows 0..47 real), B = x tile
                     // MN-major, K = 128 tokens
 #pragma unroll
                     for (int kk = 0; kk < TT / 16; ++kk)
                         ptx::tc_mma_f16(tmem + D2_COL + c * KC,
-                                        ptx::sw128_kmajor_desc(u2 + (kk >> 2) * U2_ATOM + (kk & 3) * 32),
-                                        sw128_mnmajor_desc(xs + kk * 2048, ARR_BYTES, 1024), IDESC2, (j | kk) != 0);
+                                        ptx::desc_add(desc_u2k0, u2o + (kk >> 2) * U2_ATOM + (kk & 3) * 32),
+                                        ptx::desc_add(xs, kk * 2048), IDESC2, (j | kk) != 0);
                     ptx::tc_commit(bar(BAR_D1FULL + db));
                     ptx::tc_commit(bar(BAR_EMPTY + stage));
                     if (c == NCH - 1) ptx::tc_commit(bar(BAR_UEMPTY + ub));

@@ -7,22 +7,35 @@
 // x_in = sum_i H_pre[i] x[i].
 //
 // Design (GB300, one CTA per SM, persistent):
-//   * A cluster of C CTAs owns a tile of 128 tokens at a time.  CTA c owns the
-//     D-slice [c*D/C, (c+1)*D/C) of every stream, i.e. a K-slice of 4*D/C
-//     columns of the projection, whose phi rows stay resident in shared
-//     memory as bf16 hi + lo halves (phi = hi + lo to 2^-17 relative).
-//   * A TMA producer warp streams the tile's x slice (128 tokens x 64
-//     columns per stage, 128-byte swizzle) through a ring of stages; one
-//     thread issues tcgen05.mma (M = 128 tokens, N = 48 = 24 hi + 24 lo
-//     columns, K = 16) accumulating in TMEM (two accumulators, so the next
-//     tile's MMAs overlap this tile's epilogue); four warps sum x^2 per token
-//     from the same stages.
-//   * Eight epilogue warps read the partial logits from TMEM, publish them in
-//     shared memory, and each CTA reduces 128/C tokens over the cluster's C
-//     partials through distributed shared memory, computes the gates and
-//     Sinkhorn, writes them out and pushes H_pre back to every CTA.  Each
-//     CTA then mixes its own D-slice: x is read from HBM once (TMA, kept in
-//     L2 with an evict-last hint) and read a second time from L2 for the mix.
+//   * A cluster of C CTAs owns a tile of 64 tokens at a time (small tiles keep
+//     the time between the two reads of x short enough for L2 to serve the
+//     second).  For the projection, CTA c owns the 64-column chunks c, c + C,
+//     c + 2C, ... of every stream (4*D/C columns), whose phi rows stay
+//     resident in shared memory as bf16 hi + lo halves (phi = hi + lo to
+//     2^-17 relative).  Interleaving the chunks makes the cluster read 64*C
+//     contiguous columns of each token row at a time, which DRAM serves far
+//     better than C scattered 128-byte pieces.  For the mix, CTA c owns the
+//     contiguous columns [c*D/C, (c+1)*D/C).
+//   * A TMA producer warp streams the tile's x slice through a ring of 16 KB
+//     stages (64 tokens x 64 columns of two streams, 128-byte swizzle); one
+//     thread issues tcgen05.mma with the stage's 128 rows (two streams of 64
+//     tokens) as A: against the two streams' phi chunks side by side (N = 96
+//     = 2 x (24 hi + 24 lo)), each row keeping the half of its own stream,
+//     and against the stage itself (N = 128), whose diagonal is each row's
+//     sum of x^2.  Few, large MMAs matter: a tcgen05.mma issues every few
+//     tens of cycles at best.  Accumulators live in TMEM, two of each, so
+//     the next tile's MMAs overlap this tile's epilogue.
+//   * Four gate warps read each token's two partial records (one per
+//     stream of a pair) from TMEM and push them, with the partial sum of squares, into the shared memory of the
+//     CTA that reduces that token (st.async completing on the receiver's
+//     mbarrier: no fences).  Each CTA reduces 64/C tokens over the C
+//     partials, computes H_pre first and pushes it to every CTA of the
+//     cluster the same way, and only then runs the other gates and Sinkhorn
+//     and writes them out.  Credit barriers (records read, H_pre used) let
+//     consecutive tiles overlap without a cluster-wide rendezvous.
+//   * Eight mix warps form x_in = sum_i H_pre[i] x[i] over the CTA's D-slice:
+//     x is read from HBM once (TMA, kept in L2 with an evict-last hint) and a
+//     second time, soon after, for the mix.
 //   * Every wait is bounded (about one second); on expiry the kernel latches
 //     the device error word, lets the other roles drain and returns.
 #include <cuda.h>
@@ -65,20 +78,29 @@ cudaError_t read_and_clear_device_error(unsigned* word, cudaStream_t s) {
 
 namespace tc {
 
-constexpr int TILE_M = 128;                       // tokens per tile (MMA M)
-constexpr int KW = 64;                            // K columns per stage (128 B rows)
+constexpr int TILE_M = 64;                        // tokens per tile (MMA M)
+constexpr int KW = 64;                            // K columns per chunk (128 B rows)
 constexpr int STAGES = 5;
 constexpr int NB = 48;                            // MMA N: 24 hi + 24 lo
-constexpr int STAGE_BYTES = TILE_M * KW * 2;      // 16 KB
+constexpr int SUB_BYTES = TILE_M * KW * 2;        // one stream of a stage: 8 KB
+constexpr int STAGE_BYTES = 2 * SUB_BYTES;        // a stage holds a stream pair: 16 KB
 constexpr int PHI_CHUNK_BYTES = NB * KW * 2;      // 6 KB
 constexpr int MAX_NCH = 20;                       // K-slice <= 1280 columns
 constexpr int NTHREADS = 512;                     // 16 warps
-constexpr int SS_WARP0 = 2, NSS = 2;              // x^2 warps (two token rows per lane)
-constexpr int GATE_WARP0 = 4, NGATE = 4;          // TMEM readers, cluster reduction, gates
-constexpr int MIX_WARP0 = 8, NMIX = 8;            // x_in = sum_i H_pre[i] x[i]
+constexpr int GATE_WARP0 = 2, NGATE = 4;          // TMEM readers, cluster reduction, gates
+constexpr int MIX_WARP0 = 6, NMIX = 10;           // x_in = sum_i H_pre[i] x[i]
 constexpr int REC = 25;                           // partial record: 24 logits + sum x^2
-constexpr int TMEM_COLS = 128;                    // two 64-column accumulators
-constexpr uint32_t IDESC = ptx::idesc_bf16_f32(TILE_M, NB);
+constexpr int RB = 28;                            // its stride in floats (16-byte aligned)
+constexpr uint32_t REC_TX = REC * 4;              // bytes of one record pushed to its reducer
+constexpr int TMEM_COLS = 512;                    // two (projection, Gram) accumulator pairs
+constexpr uint32_t GRAM_COL = 256;                // projection at 0 / 128, Gram at 256 / 384
+// One MMA covers a whole stage: its two 64-token stream boxes are the 128
+// rows of A.  B for the projection is the two streams' phi chunks one after
+// the other (N = 96), so rows of the first stream keep columns 0..47 and
+// rows of the second columns 48..95; the Gram product is the stage times
+// its own transpose (N = 128), whose diagonal holds the sums of squares.
+constexpr uint32_t IDESC = ptx::idesc_bf16_f32(2 * TILE_M, 2 * NB);
+constexpr uint32_t IDESC_GRAM = ptx::idesc_bf16_f32(2 * TILE_M, 2 * TILE_M);
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;  // 1 s
 
 enum : int {
@@ -86,25 +108,23 @@ enum : int {
     BAR_EMPTY = BAR_FULL + STAGES,
     BAR_ACC_FULL = BAR_EMPTY + STAGES,
     BAR_ACC_EMPTY = BAR_ACC_FULL + 2,
-    BAR_SS_FULL = BAR_ACC_EMPTY + 2,
-    BAR_SS_EMPTY = BAR_SS_FULL + 2,
-    BAR_PEER = BAR_SS_EMPTY + 2,
-    BAR_HPRE = BAR_PEER + 1,
-    BAR_MIX_DONE = BAR_HPRE + 2,
-    NBARS = BAR_MIX_DONE + 2
+    BAR_RECV = BAR_ACC_EMPTY + 2,    // this CTA's tokens: every peer's partial record arrived
+    BAR_RFREE = BAR_RECV + 1,       // every reducer of the cluster has read the last tile's records
+    BAR_HPRE = BAR_RFREE + 1,       // [2] H_pre of the tile parity arrived from the reducers
+    BAR_HFREE = BAR_HPRE + 2,       // [2] every CTA's mix has finished with that parity
+    NBARS = BAR_HFREE + 2
 };
 
 // Byte offsets inside the (1024-aligned) dynamic shared memory.
 struct Layout {
-    uint32_t phi, stages, xbuf, hpre, ssbuf, bars, misc, total;
+    uint32_t phi, stages, recv, hpre, bars, misc, total;
     __host__ __device__ static Layout make(int nch) {
         Layout L;
         L.phi = 0;
         L.stages = static_cast<uint32_t>(nch) * PHI_CHUNK_BYTES;   // multiple of 1024
-        L.xbuf = L.stages + STAGES * STAGE_BYTES;
-        L.hpre = L.xbuf + TILE_M * REC * 4;
-        L.ssbuf = L.hpre + 2 * TILE_M * 16;
-        L.bars = L.ssbuf + 2 * TILE_M * 4;
+        L.recv = L.stages + STAGES * STAGE_BYTES;    // [C senders][TILE_M / C tokens][2 halves][RB]
+        L.hpre = L.recv + 2 * TILE_M * RB * 4;
+        L.bars = L.hpre + 2 * TILE_M * 16;
         L.misc = L.bars + NBARS * 8;
         L.total = L.misc + 64 + 32 * 4;   // tmem slot, abort flag, alpha, b
         return L;
@@ -161,8 +181,7 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 16);
     float* gate_par = reinterpret_cast<float*>(smem + L.misc + 64);   // alpha[3], b[24]
-    float* xbuf = reinterpret_cast<float*>(smem + L.xbuf);
-    float* ssbuf = reinterpret_cast<float*>(smem + L.ssbuf);
+    const float* recv = reinterpret_cast<const float*>(smem + L.recv);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t c = ptx::cluster_ctarank();
@@ -172,22 +191,27 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
     const int cpd = Dc / KW;                       // chunks per stream
     const int64_t K = 4ll * D;
     constexpr int TPC = TILE_M / C;                // tokens each CTA reduces
+    const int ntl = p.ntiles > cid ? (p.ntiles - cid + ncl - 1) / ncl : 0;   // tiles of this cluster
 
     // ---- set-up: barriers, TMEM, gate parameters, resident phi slice ------
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(bar(BAR_FULL + s), 1);
-            ptx::mbar_init(bar(BAR_EMPTY + s), 1 + NSS * 32);
+            ptx::mbar_init(bar(BAR_EMPTY + s), 1);
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(bar(BAR_ACC_FULL + i), 1);
             ptx::mbar_init(bar(BAR_ACC_EMPTY + i), 128);
-            ptx::mbar_init(bar(BAR_SS_FULL + i), NSS * 32);
-            ptx::mbar_init(bar(BAR_SS_EMPTY + i), 128);
-            ptx::mbar_init(bar(BAR_HPRE + i), C);
-            ptx::mbar_init(bar(BAR_MIX_DONE + i), NMIX * 32);
+            ptx::mbar_init(bar(BAR_HPRE + i), 1);
+            ptx::mbar_init(bar(BAR_HFREE + i), C);
         }
-        ptx::mbar_init(bar(BAR_PEER), C);
+        ptx::mbar_init(bar(BAR_RECV), 1);
+        ptx::mbar_init(bar(BAR_RFREE), C);
+        // receive barriers are armed one use ahead, before any peer can send:
+        // records of the first tile, H_pre of the first two
+        if (ntl > 0) ptx::mbar_arrive_expect_tx(bar(BAR_RECV), 2 * TILE_M * REC_TX);
+        if (ntl > 0) ptx::mbar_arrive_expect_tx(bar(BAR_HPRE + 0), TILE_M * 16);
+        if (ntl > 1) ptx::mbar_arrive_expect_tx(bar(BAR_HPRE + 1), TILE_M * 16);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -205,8 +229,11 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
         const int g = item % NG;
         const int q = (item / NG) % 8;
         const int ch = item / (NG * 8);
-        const int i = ch / cpd, sub = ch % cpd;
-        const int64_t k0 = static_cast<int64_t>(i) * D + static_cast<int64_t>(c) * Dc + sub * KW + q * 8;
+        // chunk order: stream pair, chunk of the slice, stream in the pair, so
+        // that the two phi chunks one stage needs are one 96-row B operand
+        const int pr = ch / (2 * cpd), rem = ch % (2 * cpd);
+        const int sub = rem >> 1, i = 2 * pr + (rem & 1);
+        const int64_t k0 = static_cast<int64_t>(i) * D + static_cast<int64_t>(sub * C + c) * KW + q * 8;
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -234,20 +261,20 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
     if (warp == 0) {
         // ------------------------------------------------ TMA producer ----
         // The whole warp walks the loop; lane 0 waits and issues.
-        const uint64_t pol = ptx::policy_evict_last();
+        const uint64_t pol = ptx::policy_evict_normal();
         int stage = 0;
         uint32_t round = 0;
         for (int j = cid; j < p.ntiles; j += ncl) {
             const int t0 = j * TILE_M;
-            for (int ch = 0; ch < nch; ++ch) {
-                const int i = ch / cpd, sub = ch % cpd;
-                const int xk = i * D + static_cast<int>(c) * Dc + sub * KW;
+            for (int st = 0; st < nch / 2; ++st) {
+                const int pr = st / cpd, sub = st % cpd;       // stream pair, chunk of the slice
+                const int xd = (sub * C + static_cast<int>(c)) * KW;   // chunks interleaved over the cluster
                 bool ok = true;
                 if (lane == 0) ok = wait_bar<false>(bar(BAR_EMPTY + stage), (round & 1) ^ 1, abort_flag);
                 if (!__shfl_sync(FULL, ok, 0)) goto done;
                 if (lane == 0) {
                     ptx::mbar_arrive_expect_tx(bar(BAR_FULL + stage), STAGE_BYTES);
-                    ptx::tma_load_2d(sbase + L.stages + stage * STAGE_BYTES, &tmap_x, xk, t0,
+                    ptx::tma_load_3d(sbase + L.stages + stage * STAGE_BYTES, &tmap_x, xd, t0, 2 * pr,
                                      bar(BAR_FULL + stage), pol);
                 }
                 __syncwarp();
@@ -256,6 +283,8 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
         }
     } else if (warp == 1) {
         // ------------------------------------------------- MMA issuer -----
+        const uint64_t desc_stage0 = ptx::sw128_kmajor_desc(sbase + L.stages);
+        const uint64_t desc_phi0 = ptx::sw128_kmajor_desc(sbase + L.phi);
         int stage = 0;
         uint32_t round = 0;
         int it = 0;
@@ -266,18 +295,21 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
             if (lane == 0) ok = wait_bar<false>(bar(BAR_ACC_EMPTY + tb), (use & 1) ^ 1, abort_flag);
             if (!__shfl_sync(FULL, ok, 0)) goto done;
             ptx::tc_fence_after();
-            const uint32_t d_tmem = tmem_base + tb * 64;
-            for (int ch = 0; ch < nch; ++ch) {
+            const uint32_t d_tmem = tmem_base + tb * 128;
+            for (int st = 0; st < nch / 2; ++st) {
                 if (lane == 0) ok = wait_bar<false>(bar(BAR_FULL + stage), round & 1, abort_flag);
                 if (!__shfl_sync(FULL, ok, 0)) goto done;
                 ptx::tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t a0 = sbase + L.stages + stage * STAGE_BYTES;
-                    const uint32_t b0 = sbase + L.phi + ch * PHI_CHUNK_BYTES;
+                    const uint64_t da = ptx::desc_add(desc_stage0, stage * STAGE_BYTES);
+                    const uint64_t db = ptx::desc_add(desc_phi0, st * 2 * PHI_CHUNK_BYTES);
 #pragma unroll
-                    for (int kk = 0; kk < KW / 16; ++kk)
-                        ptx::tc_mma_f16(d_tmem, ptx::sw128_kmajor_desc(a0 + kk * 32),
-                                        ptx::sw128_kmajor_desc(b0 + kk * 32), IDESC, (ch | kk) != 0);
+                    for (int kk = 0; kk < KW / 16; ++kk) {
+                        const uint64_t dak = ptx::desc_add(da, kk * 32);
+                        const uint32_t acc = (st | kk) != 0;
+                        ptx::tc_mma_f16(d_tmem, dak, ptx::desc_add(db, kk * 32), IDESC, acc);
+                        ptx::tc_mma_f16(d_tmem + GRAM_COL, dak, dak, IDESC_GRAM, acc);
+                    }
                     ptx::tc_commit(bar(BAR_EMPTY + stage));
                 }
                 __syncwarp();
@@ -286,66 +318,44 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
             if (lane == 0) ptx::tc_commit(bar(BAR_ACC_FULL + tb));
             __syncwarp();
         }
-    } else if (warp < GATE_WARP0) {
-        // ------------------------------------------ sum of squares --------
-        const int r0 = (warp - SS_WARP0) * 32 + lane;   // token rows r0 and r0 + 64
-        int stage = 0;
-        uint32_t round = 0;
-        int it = 0;
-        for (int j = cid; j < p.ntiles; j += ncl, ++it) {
-            const int tb = it & 1;
-            const uint32_t use = static_cast<uint32_t>(it >> 1);
-            float ss[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-            for (int ch = 0; ch < nch; ++ch) {
-                if (!__all_sync(FULL, wait_bar<false>(bar(BAR_FULL + stage), round & 1, abort_flag))) goto done;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int r = r0 + 64 * h;
-                    const unsigned char* rowp = smem + L.stages + stage * STAGE_BYTES + r * 128;
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const uint4 v = *reinterpret_cast<const uint4*>(rowp + ((k ^ (r & 7)) * 16));
-                        float f[8];
-                        Vec<__nv_bfloat16>::unpack(v, f);
-#pragma unroll
-                        for (int e2 = 0; e2 < 8; e2 += 2) {
-                            ss[h][0] = fmaf(f[e2], f[e2], ss[h][0]);
-                            ss[h][1] = fmaf(f[e2 + 1], f[e2 + 1], ss[h][1]);
-                        }
-                    }
-                }
-                ptx::mbar_arrive(bar(BAR_EMPTY + stage));
-                if (++stage == STAGES) { stage = 0; ++round; }
-            }
-            if (!__all_sync(FULL, wait_bar<false>(bar(BAR_SS_EMPTY + tb), (use & 1) ^ 1, abort_flag))) goto done;
-            ssbuf[tb * TILE_M + r0] = ss[0][0] + ss[0][1];
-            ssbuf[tb * TILE_M + r0 + 64] = ss[1][0] + ss[1][1];
-            ptx::mbar_arrive(bar(BAR_SS_FULL + tb));
-        }
     } else if (warp < MIX_WARP0) {
         // ------------------------------------------------- gates ----------
-        // TMEM -> partial logits; publish; reduce this CTA's tokens over the
-        // cluster; gates and Sinkhorn; push H_pre to every CTA.
+        // (1) TMEM -> this CTA's partial logits and sum of squares for every
+        //     token row, pushed (st.async) to the CTA that reduces the token;
+        // (2) this CTA's TPC tokens: sum the C partials, H_pre first (pushed
+        //     to every CTA, it is all the mix waits for), then the other gates
+        //     and Sinkhorn, written out.
+        // M = 128 accumulators: lane = row; rows 0..63 are the first stream of
+        // each stage (streams 0, 2), rows 64..127 the second (1, 3).  Each
+        // row is half of a token's partial record; both halves are pushed.
         const int row = (warp & 3) * 32 + lane;        // TMEM lane quarter = warp % 4
-        const uint32_t xbuf_a = sbase + L.xbuf;
+        const int tok = row & (TILE_M - 1), hs = row / TILE_M;   // hs is the same across a warp
         const int half = lane >> 4, hl = lane & 15;    // two tokens per warp, 16 lanes each
+        const uint32_t rk = static_cast<uint32_t>(tok / TPC);   // reducer of this token
+        const uint32_t rec_dst = ptx::mapa(
+            sbase + L.recv + static_cast<uint32_t>((((c * TPC) + tok % TPC) * 2 + hs) * RB * 4), rk);
+        const uint32_t recv_bar = ptx::mapa(bar(BAR_RECV), rk);
         int it = 0;
-        bool aborted = false;
         for (int j = cid; j < p.ntiles; j += ncl, ++it) {
             const int tb = it & 1;
             const uint32_t use = static_cast<uint32_t>(it >> 1);
             const int64_t t0 = static_cast<int64_t>(j) * TILE_M;
             float z[NG];
             float ssv = 0.f;
-            bool ok = !aborted && wait_bar<false>(bar(BAR_ACC_FULL + tb), use & 1, abort_flag);
-            ok = __all_sync(FULL, ok);
+            bool ok = __all_sync(FULL, wait_bar<false>(bar(BAR_ACC_FULL + tb), use & 1, abort_flag));
             if (ok) {
                 ptx::tc_fence_after();
-                uint32_t v[3][16];
-                const uint32_t ta = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) + tb * 64;
+                uint32_t v[3][16], gd[2][16];
+                const uint32_t lanes = static_cast<uint32_t>((warp & 3) * 32) << 16;
+                const uint32_t ta = tmem_base + lanes + tb * 128 + hs * NB;
                 ptx::tmem_ld16(ta, v[0]);
                 ptx::tmem_ld16(ta + 16, v[1]);
                 ptx::tmem_ld16(ta + 32, v[2]);
+                // Gram columns 32 (warp % 4) .. +31: lane l holds row 32 (warp % 4) + l,
+                // whose diagonal entry is column l of these loads
+                const uint32_t tg = tmem_base + lanes + GRAM_COL + tb * 128 + (warp & 3) * 32;
+                ptx::tmem_ld16(tg, gd[0]);
+                ptx::tmem_ld16(tg + 16, gd[1]);
                 ptx::tmem_wait_ld();
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(bar(BAR_ACC_EMPTY + tb));
@@ -354,44 +364,37 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
                     const int h = g, l = NG + g;
                     z[g] = __uint_as_float(v[h >> 4][h & 15]) + __uint_as_float(v[l >> 4][l & 15]);
                 }
-            }
-            ok = __all_sync(FULL, ok && wait_bar<false>(bar(BAR_SS_FULL + tb), use & 1, abort_flag));
-            if (ok) {
-                ssv = ssbuf[tb * TILE_M + row];
-                ptx::mbar_arrive(bar(BAR_SS_EMPTY + tb));
-            }
-            // xbuf is reused: every CTA must have pulled the previous tile's
-            // partials (they push its H_pre only after pulling), and the
-            // H_pre buffer this tile fills must be free (mix of tile it-2).
-            if (it >= 1) {
-                const int pt = it - 1;
-                ok = __all_sync(FULL, ok && wait_bar<true>(bar(BAR_HPRE + (pt & 1)), (pt >> 1) & 1, abort_flag));
-            }
-            ok = __all_sync(FULL, ok && wait_bar<false>(bar(BAR_MIX_DONE + tb), (use & 1) ^ 1, abort_flag));
-            if (ok) {
-                float* rec = xbuf + row * REC;
 #pragma unroll
-                for (int g = 0; g < NG; ++g) rec[g] = z[g];
-                rec[NG] = ssv;
+                for (int k = 0; k < 16; ++k)
+                    if (hl == k) ssv = __uint_as_float(half ? gd[1][k] : gd[0][k]);
             }
-            if (!ok) aborted = true;
-            ptx::fence_acq_rel_cluster();
-            ptx::named_bar_sync(1, NGATE * 32);
-            if (warp == GATE_WARP0 && lane < C && !aborted) ptx::mbar_arrive_remote(ptx::mapa(bar(BAR_PEER), lane));
-            if (!__all_sync(FULL, !aborted && wait_bar<true>(bar(BAR_PEER), it & 1, abort_flag))) aborted = true;
-            if (!aborted) {
+            // the reducers have read the previous tile's records
+            if (it >= 1) ok = ok && __all_sync(FULL, wait_bar<true>(bar(BAR_RFREE), (it - 1) & 1, abort_flag));
+            if (ok) {
+#pragma unroll
+                for (int v4 = 0; v4 < NG / 4; ++v4)
+                    ptx::st_async_v4(rec_dst + 16 * v4, z[4 * v4], z[4 * v4 + 1], z[4 * v4 + 2], z[4 * v4 + 3],
+                                     recv_bar);
+                ptx::st_async_b32(rec_dst + 4 * NG, ssv, recv_bar);
+            }
+            // H_pre of this parity is free at every CTA (mix of tile it-2 done)
+            if (it >= 2) ok = ok && __all_sync(FULL, wait_bar<true>(bar(BAR_HFREE + tb), (use - 1) & 1, abort_flag));
+            ok = ok && __all_sync(FULL, wait_bar<true>(bar(BAR_RECV), it & 1, abort_flag));
+            if (ok) {
                 for (int tt0 = (warp - GATE_WARP0) * 2; tt0 < TPC; tt0 += NGATE * 2) {
                     const int tt = tt0 + half;
                     const bool real = tt < TPC;
                     const int r = static_cast<int>(c) * TPC + (real ? tt : 0);
                     float va = 0.f, vb = 0.f;
                     if (real) {
-                        const uint32_t a = xbuf_a + static_cast<uint32_t>((r * REC + hl) * 4);
 #pragma unroll
-                        for (int s = 0; s < C; ++s) va += ptx::ld_cluster_f32(ptx::mapa(a, s));
-                        if (hl + 16 < REC) {
+                        for (int s = 0; s < C; ++s) {
 #pragma unroll
-                            for (int s = 0; s < C; ++s) vb += ptx::ld_cluster_f32(ptx::mapa(a + 64, s));
+                            for (int h2 = 0; h2 < 2; ++h2) {
+                                const float* rec = recv + ((s * TPC + tt) * 2 + h2) * RB;
+                                va += rec[hl];
+                                if (hl + 16 < REC) vb += rec[hl + 16];
+                            }
                         }
                     }
                     float pj[NG];
@@ -401,32 +404,46 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
                     const float inv = 1.0f / sqrtf(sq / static_cast<float>(K) + p.eps);
 #pragma unroll
                     for (int g = 0; g < NG; ++g) pj[g] *= inv;
-                    float hp[4], hq[4], hr[16];
-                    token_gates(pj, gate_par, gate_par + 3, p.iters, hp, hq, hr);
+                    // the pre gates (same expression as in token_gates)
+                    float hp[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) hp[i] = sigmoid_f(fmaf(gate_par[0], pj[i], gate_par[3 + i]));
+                    if (real && hl < C)
+                        ptx::st_async_v4(ptx::mapa(sbase + L.hpre + static_cast<uint32_t>((tb * TILE_M + r) * 16),
+                                                   static_cast<uint32_t>(hl)),
+                                         hp[0], hp[1], hp[2], hp[3],
+                                         ptx::mapa(bar(BAR_HPRE + tb), static_cast<uint32_t>(hl)));
+                    float hp2[4], hq[4], hr[16];
+                    token_gates(pj, gate_par, gate_par + 3, p.iters, hp2, hq, hr);
                     const int64_t t = t0 + r;
                     if (real && t < p.T) {
-                        if (hl < 6)
-                            reinterpret_cast<float4*>(p.proj + t * NG)[hl] =
-                                make_float4(pj[4 * hl], pj[4 * hl + 1], pj[4 * hl + 2], pj[4 * hl + 3]);
+                        // lane hl writes one float4 of the token's outputs; the
+                        // value is picked with constant indices so that pj and
+                        // hr (Sinkhorn's working matrix) stay in registers
+                        float4 o = make_float4(hp[0], hp[1], hp[2], hp[3]);
+#pragma unroll
+                        for (int v = 0; v < NG / 4; ++v)
+                            if (hl == v) o = make_float4(pj[4 * v], pj[4 * v + 1], pj[4 * v + 2], pj[4 * v + 3]);
+                        if (hl == 8) o = make_float4(hq[0], hq[1], hq[2], hq[3]);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            if (hl == 9 + v) o = make_float4(hr[4 * v], hr[4 * v + 1], hr[4 * v + 2], hr[4 * v + 3]);
+                        if (hl < 6) reinterpret_cast<float4*>(p.proj + t * NG)[hl] = o;
                         else if (hl == 6) p.inv_rms[t] = inv;
-                        else if (hl == 7) reinterpret_cast<float4*>(p.H_pre)[t] = make_float4(hp[0], hp[1], hp[2], hp[3]);
-                        else if (hl == 8) reinterpret_cast<float4*>(p.H_post)[t] = make_float4(hq[0], hq[1], hq[2], hq[3]);
-                        else if (hl < 13) {
-                            const int v = hl - 9;
-                            reinterpret_cast<float4*>(p.H_res + t * 16)[v] =
-                                make_float4(hr[4 * v], hr[4 * v + 1], hr[4 * v + 2], hr[4 * v + 3]);
-                        }
-                    }
-                    if (real && hl < C) {
-                        const uint32_t dst = sbase + L.hpre + static_cast<uint32_t>((tb * TILE_M + r) * 16);
-                        ptx::st_cluster_v4(ptx::mapa(dst, hl), hp[0], hp[1], hp[2], hp[3]);
-                        ptx::fence_acq_rel_cluster();
+                        else if (hl == 7) reinterpret_cast<float4*>(p.H_pre)[t] = o;
+                        else if (hl == 8) reinterpret_cast<float4*>(p.H_post)[t] = o;
+                        else if (hl < 13) reinterpret_cast<float4*>(p.H_res + t * 16)[hl - 9] = o;
                     }
                 }
             }
-            ptx::named_bar_sync(1, NGATE * 32);
-            if (warp == GATE_WARP0 && lane < C && !aborted) ptx::mbar_arrive_remote(ptx::mapa(bar(BAR_HPRE + tb), lane));
-            if (ptx::named_bar_or(2, NGATE * 32, aborted)) break;
+            // every gate warp is done with the records: arm the barrier for the
+            // next tile's, then tell every sender the buffer is free
+            if (ptx::named_bar_or(1, NGATE * 32, !ok)) break;
+            if (warp == GATE_WARP0) {
+                if (lane == 0 && it + 1 < ntl) ptx::mbar_arrive_expect_tx(bar(BAR_RECV), 2 * TILE_M * REC_TX);
+                __syncwarp();
+                if (lane < C) ptx::mbar_arrive_remote(ptx::mapa(bar(BAR_RFREE), static_cast<uint32_t>(lane)));
+            }
         }
     } else {
         // --------------------------------------------------- mix ----------
@@ -438,10 +455,10 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
             const int tb = it & 1;
             const uint32_t use = static_cast<uint32_t>(it >> 1);
             const int64_t t0 = static_cast<int64_t>(j) * TILE_M;
-            if (!__all_sync(FULL, wait_bar<true>(bar(BAR_HPRE + tb), use & 1, abort_flag))) break;
+            const bool ok = __all_sync(FULL, wait_bar<true>(bar(BAR_HPRE + tb), use & 1, abort_flag));
             const float4* hb = reinterpret_cast<const float4*>(smem + L.hpre) + tb * TILE_M;
             const int qpt = Dc / 8;
-            const int items = TILE_M * qpt;
+            const int items = ok ? TILE_M * qpt : 0;
             for (int base = 0; base < items; base += NMIX * 32 * 4) {
                 uint4 xv[4][4];
                 int64_t tok[4];
@@ -475,7 +492,14 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
                     }
                 }
             }
-            ptx::mbar_arrive(bar(BAR_MIX_DONE + tb));
+            // every mix thread is done with this parity's H_pre: arm it for
+            // tile it + 2, then free it at every reducer
+            if (ptx::named_bar_or(3, NMIX * 32, !ok)) break;
+            if (warp == MIX_WARP0) {
+                if (lane == 0 && it + 2 < ntl) ptx::mbar_arrive_expect_tx(bar(BAR_HPRE + tb), TILE_M * 16);
+                __syncwarp();
+                if (lane < C) ptx::mbar_arrive_remote(ptx::mapa(bar(BAR_HFREE + tb), static_cast<uint32_t>(lane)));
+            }
         }
     }
 done:
@@ -604,12 +628,14 @@ cudaError_t launch_pre_tc(const void* x, const float* phi, const float* b, const
     auto encode = tc::encode_fn();
     if (C == 0 || encode == nullptr) return cudaErrorNotSupported;
     const int64_t K = 4 * D;
+    // x as (d, token, stream): a box is 64 columns x 64 tokens x 2 streams,
+    // laid out in shared memory as [stream][token][64 columns]
     CUtensorMap tm;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(T)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K * 2)};
-    const cuuint32_t box[2] = {tc::KW, tc::TILE_M};
-    const cuuint32_t estr[2] = {1, 1};
-    if (encode(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(T), 4};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K * 2), static_cast<cuuint64_t>(D * 2)};
+    const cuuint32_t box[3] = {tc::KW, tc::TILE_M, 2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (encode(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;

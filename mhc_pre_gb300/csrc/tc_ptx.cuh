@@ -113,6 +113,21 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, f
                  "f"(c), "f"(d)
                  : "memory");
 }
+// Stores into another CTA's shared memory (`caddr` from mapa) that complete
+// their byte count on that CTA's mbarrier `cbar` (also from mapa): the
+// receiver sees the data once the barrier's phase completes, with no fence.
+__device__ __forceinline__ void st_async_v4(uint32_t caddr, float a, float b, float c, float d, uint32_t cbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::
+                     "r"(caddr),
+                 "r"(__float_as_uint(a)), "r"(__float_as_uint(b)), "r"(__float_as_uint(c)), "r"(__float_as_uint(d)),
+                 "r"(cbar)
+                 : "memory");
+}
+__device__ __forceinline__ void st_async_b32(uint32_t caddr, float a, uint32_t cbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(caddr),
+                 "r"(__float_as_uint(a)), "r"(cbar)
+                 : "memory");
+}
 __device__ __forceinline__ void fence_acq_rel_cluster() {
     asm volatile("fence.acq_rel.cluster;" ::: "memory");
 }
@@ -140,6 +155,11 @@ __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, boo
 __device__ __forceinline__ uint64_t policy_evict_last() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
 __device__ __forceinline__ uint64_t policy_evict_first() {
@@ -273,6 +293,13 @@ __device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t addr, uint32_t l
 __device__ __forceinline__ uint32_t sw128_off(int row, int col) {
     return static_cast<uint32_t>(row * 128 + (((col >> 3) ^ (row & 7)) << 4) + (col & 7) * 2);
 }
+
+// The same descriptor moved by `bytes` (a multiple of 16) in shared memory.
+// Only the start-address field (address >> 4, 14 bits) changes: shared
+// addresses stay below 256 KB, so the add never carries into other fields.
+// Building descriptors once and moving them this way keeps the MMA-issuing
+// thread's loop short (a tcgen05.mma issues every few tens of cycles).
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
 // Instruction descriptor of kind::f16 with bf16 A and B, fp32 D, both
 // operands K-major, shape M x N.
