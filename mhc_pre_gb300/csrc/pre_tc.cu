@@ -87,8 +87,10 @@ constexpr int STAGE_BYTES = 2 * SUB_BYTES;        // a stage holds a stream pair
 constexpr int PHI_CHUNK_BYTES = NB * KW * 2;      // 6 KB
 constexpr int MAX_NCH = 20;                       // K-slice <= 1280 columns
 constexpr int NTHREADS = 512;                     // 16 warps
-constexpr int GATE_WARP0 = 2, NGATE = 4;          // TMEM readers, cluster reduction, gates
-constexpr int MIX_WARP0 = 6, NMIX = 10;           // x_in = sum_i H_pre[i] x[i]
+constexpr int GATE_WARP0 = 2, NGATE = 4;          // TMEM readers, cluster reduction, H_pre
+constexpr int SK_WARP = 6;                        // Sinkhorn, other gates, outputs
+constexpr int MIX_WARP0 = 7, NMIX = 9;            // x_in = sum_i H_pre[i] x[i]
+constexpr int SKF = 28;                           // hand-off record: proj[24], inv_rms (floats)
 constexpr int REC = 25;                           // partial record: 24 logits + sum x^2
 constexpr int RB = 28;                            // its stride in floats (16-byte aligned)
 constexpr uint32_t REC_TX = REC * 4;              // bytes of one record pushed to its reducer
@@ -112,19 +114,22 @@ enum : int {
     BAR_RFREE = BAR_RECV + 1,       // every reducer of the cluster has read the last tile's records
     BAR_HPRE = BAR_RFREE + 1,       // [2] H_pre of the tile parity arrived from the reducers
     BAR_HFREE = BAR_HPRE + 2,       // [2] every CTA's mix has finished with that parity
-    NBARS = BAR_HFREE + 2
+    BAR_SKFULL = BAR_HFREE + 2,     // [2] reduced tokens handed to the Sinkhorn warp
+    BAR_SKEMPTY = BAR_SKFULL + 2,   // [2] the Sinkhorn warp is done with them
+    NBARS = BAR_SKEMPTY + 2
 };
 
 // Byte offsets inside the (1024-aligned) dynamic shared memory.
 struct Layout {
-    uint32_t phi, stages, recv, hpre, bars, misc, total;
-    __host__ __device__ static Layout make(int nch) {
+    uint32_t phi, stages, recv, hpre, sk, bars, misc, total;
+    __host__ __device__ static Layout make(int nch, int tpc) {
         Layout L;
         L.phi = 0;
         L.stages = static_cast<uint32_t>(nch) * PHI_CHUNK_BYTES;   // multiple of 1024
         L.recv = L.stages + STAGES * STAGE_BYTES;    // [C senders][TILE_M / C tokens][2 halves][RB]
         L.hpre = L.recv + 2 * TILE_M * RB * 4;
-        L.bars = L.hpre + 2 * TILE_M * 16;
+        L.sk = L.hpre + 2 * TILE_M * 16;              // [2][tpc][SKF]
+        L.bars = L.sk + 2 * tpc * SKF * 4;
         L.misc = L.bars + NBARS * 8;
         L.total = L.misc + 64 + 32 * 4;   // tmem slot, abort flag, alpha, b
         return L;
@@ -174,7 +179,8 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const Layout L = Layout::make(p.nch);
+    constexpr int TPC = TILE_M / C;                // tokens each CTA reduces
+    const Layout L = Layout::make(p.nch, TPC);
     const uint32_t sbase = ptx::smem_u32(smem);
     const uint32_t bars = sbase + L.bars;
     auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
@@ -190,7 +196,6 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
     const int D = p.D, Dc = p.Dc, nch = p.nch;
     const int cpd = Dc / KW;                       // chunks per stream
     const int64_t K = 4ll * D;
-    constexpr int TPC = TILE_M / C;                // tokens each CTA reduces
     const int ntl = p.ntiles > cid ? (p.ntiles - cid + ncl - 1) / ncl : 0;   // tiles of this cluster
 
     // ---- set-up: barriers, TMEM, gate parameters, resident phi slice ------
@@ -204,6 +209,8 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
             ptx::mbar_init(bar(BAR_ACC_EMPTY + i), 128);
             ptx::mbar_init(bar(BAR_HPRE + i), 1);
             ptx::mbar_init(bar(BAR_HFREE + i), C);
+            ptx::mbar_init(bar(BAR_SKFULL + i), 1);
+            ptx::mbar_init(bar(BAR_SKEMPTY + i), 1);
         }
         ptx::mbar_init(bar(BAR_RECV), 1);
         ptx::mbar_init(bar(BAR_RFREE), C);
@@ -318,13 +325,13 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
             if (lane == 0) ptx::tc_commit(bar(BAR_ACC_FULL + tb));
             __syncwarp();
         }
-    } else if (warp < MIX_WARP0) {
+    } else if (warp < SK_WARP) {
         // ------------------------------------------------- gates ----------
         // (1) TMEM -> this CTA's partial logits and sum of squares for every
         //     token row, pushed (st.async) to the CTA that reduces the token;
-        // (2) this CTA's TPC tokens: sum the C partials, H_pre first (pushed
-        //     to every CTA, it is all the mix waits for), then the other gates
-        //     and Sinkhorn, written out.
+        // (2) this CTA's TPC tokens: sum the partials, H_pre (pushed to every
+        //     CTA, it is all the mix waits for), and hand the projection to
+        //     the Sinkhorn warp for the other gates and the outputs.
         // M = 128 accumulators: lane = row; rows 0..63 are the first stream of
         // each stage (streams 0, 2), rows 64..127 the second (1, 3).  Each
         // row is half of a token's partial record; both halves are pushed.
@@ -339,7 +346,6 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
         for (int j = cid; j < p.ntiles; j += ncl, ++it) {
             const int tb = it & 1;
             const uint32_t use = static_cast<uint32_t>(it >> 1);
-            const int64_t t0 = static_cast<int64_t>(j) * TILE_M;
             float z[NG];
             float ssv = 0.f;
             bool ok = __all_sync(FULL, wait_bar<false>(bar(BAR_ACC_FULL + tb), use & 1, abort_flag));
@@ -379,6 +385,8 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
             }
             // H_pre of this parity is free at every CTA (mix of tile it-2 done)
             if (it >= 2) ok = ok && __all_sync(FULL, wait_bar<true>(bar(BAR_HFREE + tb), (use - 1) & 1, abort_flag));
+            // the Sinkhorn warp is done with this parity's hand-off (tile it-2)
+            if (it >= 2) ok = ok && __all_sync(FULL, wait_bar<false>(bar(BAR_SKEMPTY + tb), (use - 1) & 1, abort_flag));
             ok = ok && __all_sync(FULL, wait_bar<true>(bar(BAR_RECV), it & 1, abort_flag));
             if (ok) {
                 for (int tt0 = (warp - GATE_WARP0) * 2; tt0 < TPC; tt0 += NGATE * 2) {
@@ -413,26 +421,14 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
                                                    static_cast<uint32_t>(hl)),
                                          hp[0], hp[1], hp[2], hp[3],
                                          ptx::mapa(bar(BAR_HPRE + tb), static_cast<uint32_t>(hl)));
-                    float hp2[4], hq[4], hr[16];
-                    token_gates(pj, gate_par, gate_par + 3, p.iters, hp2, hq, hr);
-                    const int64_t t = t0 + r;
-                    if (real && t < p.T) {
-                        // lane hl writes one float4 of the token's outputs; the
-                        // value is picked with constant indices so that pj and
-                        // hr (Sinkhorn's working matrix) stay in registers
-                        float4 o = make_float4(hp[0], hp[1], hp[2], hp[3]);
+                    if (real && hl < SKF / 4) {
+                        // hand-off record: proj[24], inv_rms (picked with constant
+                        // indices so that pj stays in registers)
+                        float4 o = make_float4(inv, 0.f, 0.f, 0.f);
 #pragma unroll
                         for (int v = 0; v < NG / 4; ++v)
                             if (hl == v) o = make_float4(pj[4 * v], pj[4 * v + 1], pj[4 * v + 2], pj[4 * v + 3]);
-                        if (hl == 8) o = make_float4(hq[0], hq[1], hq[2], hq[3]);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            if (hl == 9 + v) o = make_float4(hr[4 * v], hr[4 * v + 1], hr[4 * v + 2], hr[4 * v + 3]);
-                        if (hl < 6) reinterpret_cast<float4*>(p.proj + t * NG)[hl] = o;
-                        else if (hl == 6) p.inv_rms[t] = inv;
-                        else if (hl == 7) reinterpret_cast<float4*>(p.H_pre)[t] = o;
-                        else if (hl == 8) reinterpret_cast<float4*>(p.H_post)[t] = o;
-                        else if (hl < 13) reinterpret_cast<float4*>(p.H_res + t * 16)[hl - 9] = o;
+                        reinterpret_cast<float4*>(smem + L.sk)[(tb * TPC + tt) * (SKF / 4) + hl] = o;
                     }
                 }
             }
@@ -440,10 +436,65 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
             // next tile's, then tell every sender the buffer is free
             if (ptx::named_bar_or(1, NGATE * 32, !ok)) break;
             if (warp == GATE_WARP0) {
+                if (lane == 0) ptx::mbar_arrive(bar(BAR_SKFULL + tb));
                 if (lane == 0 && it + 1 < ntl) ptx::mbar_arrive_expect_tx(bar(BAR_RECV), 2 * TILE_M * REC_TX);
                 __syncwarp();
                 if (lane < C) ptx::mbar_arrive_remote(ptx::mapa(bar(BAR_RFREE), static_cast<uint32_t>(lane)));
             }
+        }
+    } else if (warp == SK_WARP) {
+        // ----------------------------------------- Sinkhorn and outputs ---
+        // The other gates of this CTA's reduced tokens (H_post, Sinkhorn for
+        // H_res) and every per-token output, off the mix's critical path.
+        // Eight lanes per token; lane l8 writes outputs l8 and l8 + 8 of the
+        // 13 float4-sized pieces: proj[0..5], inv_rms, H_pre, H_post, H_res[0..3].
+        const int l8 = lane & 7;
+        int it = 0;
+        for (int j = cid; j < p.ntiles; j += ncl, ++it) {
+            const int tb = it & 1;
+            const uint32_t use = static_cast<uint32_t>(it >> 1);
+            if (!__all_sync(FULL, wait_bar<false>(bar(BAR_SKFULL + tb), use & 1, abort_flag))) break;
+            const int64_t t0 = static_cast<int64_t>(j) * TILE_M;
+            for (int tt0 = 0; tt0 < TPC; tt0 += 4) {
+                const int tt = tt0 + (lane >> 3);
+                const bool real = tt < TPC;
+                float pj[NG], inv = 0.f;
+#pragma unroll
+                for (int g = 0; g < NG; ++g) pj[g] = 0.f;
+                if (real) {
+                    const float4* rec = reinterpret_cast<const float4*>(smem + L.sk) + (tb * TPC + tt) * (SKF / 4);
+#pragma unroll
+                    for (int v = 0; v < NG / 4; ++v) {
+                        const float4 a = rec[v];
+                        pj[4 * v] = a.x; pj[4 * v + 1] = a.y; pj[4 * v + 2] = a.z; pj[4 * v + 3] = a.w;
+                    }
+                    inv = rec[NG / 4].x;
+                }
+                float hp[4], hq[4], hr[16];
+                token_gates(pj, gate_par, gate_par + 3, p.iters, hp, hq, hr);
+                const int64_t t = t0 + static_cast<int>(c) * TPC + tt;
+                if (real && t < p.T) {
+#pragma unroll
+                    for (int rep = 0; rep < 2; ++rep) {
+                        const int k = l8 + 8 * rep;
+                        float4 o = make_float4(hp[0], hp[1], hp[2], hp[3]);
+#pragma unroll
+                        for (int v = 0; v < NG / 4; ++v)
+                            if (k == v) o = make_float4(pj[4 * v], pj[4 * v + 1], pj[4 * v + 2], pj[4 * v + 3]);
+                        if (k == 8) o = make_float4(hq[0], hq[1], hq[2], hq[3]);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            if (k == 9 + v) o = make_float4(hr[4 * v], hr[4 * v + 1], hr[4 * v + 2], hr[4 * v + 3]);
+                        if (k < 6) reinterpret_cast<float4*>(p.proj + t * NG)[k] = o;
+                        else if (k == 6) p.inv_rms[t] = inv;
+                        else if (k == 7) reinterpret_cast<float4*>(p.H_pre)[t] = o;
+                        else if (k == 8) reinterpret_cast<float4*>(p.H_post)[t] = o;
+                        else if (k < 13) reinterpret_cast<float4*>(p.H_res + t * 16)[k - 9] = o;
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(BAR_SKEMPTY + tb));
         }
     } else {
         // --------------------------------------------------- mix ----------
@@ -544,7 +595,7 @@ int cluster_for(int64_t D) {
     return 0;
 }
 
-size_t smem_bytes(int nch) { return Layout::make(nch).total + 1024; }
+size_t smem_bytes(int nch, int C) { return Layout::make(nch, TILE_M / C).total + 1024; }
 
 template <int C>
 int max_clusters(size_t smem) {
@@ -557,7 +608,7 @@ int max_clusters(size_t smem) {
         int n = 0;
         auto k = pre_tc_kernel<C>;
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem_bytes(MAX_NCH))) != cudaSuccess ||
+                                 static_cast<int>(smem_bytes(MAX_NCH, C))) != cudaSuccess ||
             (C > 8 && cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)) {
             cache[dev] = 0;
             return;
@@ -565,7 +616,7 @@ int max_clusters(size_t smem) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(C * 64);
         cfg.blockDim = dim3(NTHREADS);
-        cfg.dynamicSmemBytes = smem_bytes(MAX_NCH);
+        cfg.dynamicSmemBytes = smem_bytes(MAX_NCH, C);
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = C;
@@ -617,7 +668,7 @@ bool pre_tc_supports(int64_t T, int64_t D) {
     const int C = tc::cluster_for(D);
     if (C == 0 || tc::encode_fn() == nullptr) return false;
     const int nch = static_cast<int>(4 * D / C / tc::KW);
-    return tc::max_clusters_for(C, tc::smem_bytes(nch)) > 0;
+    return tc::max_clusters_for(C, tc::smem_bytes(nch, C)) > 0;
 }
 
 cudaError_t launch_pre_tc(const void* x, const float* phi, const float* b, const float* alpha,
@@ -657,7 +708,7 @@ cudaError_t launch_pre_tc(const void* x, const float* phi, const float* b, const
     prm.H_res = H_res;
     prm.proj = proj;
     prm.inv_rms = inv_rms;
-    const size_t smem = tc::smem_bytes(prm.nch);
+    const size_t smem = tc::smem_bytes(prm.nch, C);
     int ncl = tc::max_clusters_for(C, smem);
     if (ncl <= 0) return cudaErrorNotSupported;
     if (ncl > prm.ntiles) ncl = prm.ntiles;
