@@ -185,8 +185,9 @@ mhc_status mhc_pre_bwd(mhc_dtype dt, const void* g_in, const float* dH_post,
  * Limits and behaviour:
  *   - The array holds MHC_PRE_BWD_NOALLOC_SCRATCH_BYTES (16 MiB) on every GPU
  *     that loads the library, until the process exits.  The call returns
- *     MHC_ERR_UNSUPPORTED when T * 256 bytes of per-token records plus one
- *     4*D x 24 float32 partial of dphi exceed it (for D = 5120: T <= 57,856).
+ *     MHC_ERR_UNSUPPORTED when T * 256 bytes of per-token records, one
+ *     4*D x 24 float32 partial of dphi and D * 256 bytes of bf16 phi blocks
+ *     exceed it (for D = 5120: T <= 52,736).
  *   - The first call on a device looks up the array's device address on that
  *     device (cudaGetSymbolAddress); make that first call before any stream
  *     capture.

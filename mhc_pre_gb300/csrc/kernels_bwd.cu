@@ -424,7 +424,8 @@ PreBwdPlan pre_bwd_plan(int64_t T, int64_t D) {
     p.tb = (T + nb - 1) / nb;
     p.rec_bytes = static_cast<size_t>(T) * REC * sizeof(float);
     p.part_bytes = static_cast<size_t>(nb) * K * NG * sizeof(float);
-    p.total_bytes = T > 0 ? p.rec_bytes + p.part_bytes : 0;
+    p.phi_bytes = pre_bwd_fused_phi_bytes(D);
+    p.total_bytes = T > 0 ? p.rec_bytes + p.part_bytes + p.phi_bytes : 0;
     return p;
 }
 
@@ -446,8 +447,9 @@ cudaError_t launch_post_bwd(bool bf16, const void* g, const void* x, const void*
 }
 
 // The pre backward with room for at most nb dphi partials (scratch = T * REC
-// floats of records, then nb * K * NG floats of partials): launch_pre_bwd
-// passes the plan's nb, the entry point with a fixed scratch array its own.
+// floats of records, nb * K * NG floats of partials, then D * 256 bytes of
+// bf16 phi blocks): launch_pre_bwd passes the plan's nb, the entry point with
+// a fixed scratch array its own.
 cudaError_t launch_pre_bwd_blocks(bool bf16, const void* g_in, const float* dH_post,
                                   const float* dH_res, const void* x, const float* phi,
                                   const float* b, const float* alpha, const float* proj,
@@ -466,8 +468,10 @@ cudaError_t launch_pre_bwd_blocks(bool bf16, const void* g_in, const float* dH_p
         // one pass: per-token gate backward first (it does not need dH_pre),
         // then the cluster kernel finds dH_pre and does the rest
         pre_bwd_token_kernel<<<gt, 128, 0, s>>>(dH_post, dH_res, b, alpha, proj, inv_rms, T, K, iters, 0, rec);
+        void* phi2 = static_cast<char*>(ws) + static_cast<size_t>(T) * REC * sizeof(float) +
+                     static_cast<size_t>(nb) * K * NG * sizeof(float);
         const cudaError_t e = launch_pre_bwd_fused_main(g_in, x, phi, proj, alpha, rec, T, D, nb, dx, part,
-                                                        &nparts, s);
+                                                        phi2, &nparts, s);
         if (e != cudaSuccess) return e;
     } else if (bf16) {
         pre_bwd_dots_kernel<__nv_bfloat16><<<gw, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(g_in),

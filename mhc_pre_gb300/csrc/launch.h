@@ -25,6 +25,7 @@ struct PreBwdPlan {
     int64_t tb;          // tokens per block
     size_t rec_bytes;    // T * REC floats
     size_t part_bytes;   // nb * K * NG floats
+    size_t phi_bytes;    // bf16 phi blocks of the one-pass kernel
     size_t total_bytes;
 };
 PreBwdPlan pre_bwd_plan(int64_t T, int64_t D);
@@ -62,11 +63,13 @@ cudaError_t launch_pre_bwd_blocks(bool bf16, const void* g_in, const float* dH_p
 // dH_pre dots, the rest of u and the RMSNorm coefficient, dx and the dphi
 // partials (one per cluster, at most `max_parts`).  It expects records from
 // the per-token kernel run without dH_pre and writes their pre-gate parts.
+// It first packs phi as bf16 pair blocks into `phi2` (pre_bwd_fused_phi_bytes).
 bool pre_bwd_fused_supports(int64_t T, int64_t D);
+size_t pre_bwd_fused_phi_bytes(int64_t D);
 cudaError_t launch_pre_bwd_fused_main(const void* g_in, const void* x, const float* phi,
                                       const float* proj, const float* alpha, float* rec,
                                       int64_t T, int64_t D, int64_t max_parts, void* dx,
-                                      float* part, int64_t* nparts, cudaStream_t s);
+                                      float* part, void* phi2, int64_t* nparts, cudaStream_t s);
 
 // Tensor-core main step of the pre backward (bf16; pre_bwd_tc.cu).
 bool pre_bwd_tc_supports(int64_t T, int64_t D);

@@ -120,7 +120,7 @@ int mhc_kernel_launches(const char* op, mhc_dtype dt, int64_t T, int n, int64_t 
     if (T == 0) return 0;
     if (strcmp(op, "mhc_pre") == 0) return dt == MHC_BF16 && mhc::pre_tc_supports(T, D) ? 1 : 2;
     if (strcmp(op, "mhc_post") == 0 || strcmp(op, "mhc_post_bwd") == 0) return 1;
-    if (strcmp(op, "mhc_pre_bwd") == 0) return dt == MHC_BF16 && mhc::pre_bwd_fused_supports(T, D) ? 4 : 5;
+    if (strcmp(op, "mhc_pre_bwd") == 0) return 5;   // both paths: 5 launches
     return -1;
 }
 

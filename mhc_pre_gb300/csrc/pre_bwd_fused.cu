@@ -16,15 +16,17 @@
 //
 // Design (GB300, one CTA per SM, persistent):
 //   * A cluster of C CTAs owns a tile of 64 tokens at a time; CTA r owns the
-//     columns d in [r*Dc, (r+1)*Dc) of every stream (Dc = 64 * nck).
-//   * First pass: TMA brings the tile's x (one 32 KB box: 4 streams x 64
-//     tokens x 64 columns) and g_in (8 KB) per 64-column chunk; four warps
-//     sum g_in * x[i] per token.  The C partial dot products of each token
-//     are exchanged through distributed shared memory, and two warps finish
-//     u and coef for the tile.
-//   * Second pass: the same boxes again (now from L2), while the first pass
-//     of the next tile and its exchange run ahead.  One thread issues
-//     tcgen05.mma:
+//     64-column chunks r, r + C, r + 2C, ... of every stream (nck of them),
+//     so that the cluster reads 64 C contiguous columns of a row at a time.
+//   * First pass (dot warps): TMA brings, per chunk and stream pair, a 16 KB
+//     x box (64 tokens x 64 columns x 2 streams) and the 8 KB g_in box into
+//     a ring of its own; four warps sum g_in * x[i] per token.  The C
+//     partial dot products of each token are exchanged through distributed
+//     shared memory and two warps finish u and coef for the tile.
+//   * Second pass (MMA and epilogue): a second ring brings, per chunk and
+//     stream pair, the same x box again (now from L2), the pair's phi block
+//     (bf16, packed once per launch in the workspace) and the g_in box.  One
+//     thread issues tcgen05.mma:
 //       D1 = U' . PHI2^T  (M = 128 = 64 tokens x 2 streams, N = 64, K = 64):
 //         U' holds u in the first 32 K-columns of rows 0..63 and in the last
 //         32 of rows 64..127, PHI2 holds phi of stream 2p in its first 32
@@ -33,14 +35,17 @@
 //       D2 += X^T . U     (M = 128 = 2 streams x 64 columns, read MN-major
 //         from the box, N = 32 (24 logits), K = 64 tokens): the dphi partial
 //         of the CTA's columns, resident in TMEM for the whole kernel.
-//     Eight epilogue warps (one token and stream per thread, as the TMEM
-//     lane layout gives) form the increment H_pre g_in + D1 + coef x in bf16
-//     over the x rows it came from, and one thread per stream pair adds that
+//     Four epilogue warps per stream pair (one token and stream per thread,
+//     as the TMEM lane layout gives) form the increment H_pre g_in + D1 +
+//     coef x in bf16 over the x rows it came from, and one thread adds that
 //     box to dx with a TMA reduction (the add happens in L2), so dx is never
 //     staged on chip.
-//   * phi (bf16, 24 logits padded to 32) stays in shared memory; u enters
-//     both products in bf16, far inside the tolerance of the bf16 dx and of
-//     the dphi sums.
+//   * With phi streamed, shared memory holds two rings deep enough for the
+//     two passes to run side by side; the producer serves both without
+//     blocking and issues a tile's second-pass boxes only after its first
+//     pass ones, so that they come from L2.
+//   * u enters both products in bf16, far inside the tolerance of the bf16
+//     dx and of the dphi sums.
 //   * Every wait is bounded (about one second); on expiry the kernel latches
 //     its device error word and returns.
 #include <cuda.h>
@@ -73,39 +78,40 @@ namespace bwdfu {
 constexpr int TT = 64;                      // tokens per tile
 constexpr int KC = 64;                      // columns per chunk
 constexpr int MAX_NCK = 5;                  // chunks per stream per CTA
-constexpr int XSLOTS = 3;                   // ring of x / dx boxes
-constexpr int GSLOTS = 3;                   // ring of g_in boxes
-constexpr int SUB = TT * 128;               // one stream of a box: 64 tokens x 128 B
-constexpr int XBOX = 4 * SUB;               // 32 KB
-constexpr int GBOX = SUB;                   // 8 KB
-constexpr int PHI_BLK = KC * 128;           // 64 columns x [phi stream 2p | phi stream 2p+1]
+constexpr int SUB = TT * 128;               // one stream of a box: 64 tokens x 128 B = 8 KB
+constexpr int PBOX = 2 * SUB;               // x box of a stream pair: 16 KB
+constexpr int GBOX = SUB;                   // g_in box: 8 KB
+constexpr int PHIB = KC * 128;              // phi block of a pair: 64 columns x [phi 2p | phi 2p+1]
+constexpr int ASLOTS = 3;                   // first pass: [x pair box | g_in box]
+constexpr int A_SLOT = PBOX + GBOX;         // 24 KB
+constexpr int BSLOTS = 4;                   // second pass: [x pair box | phi block | g_in box]
+constexpr int B_SLOT = PBOX + PHIB + GBOX;  // 32 KB
 constexpr int NTHREADS = 512;               // 16 warps
 constexpr int DOT_WARP0 = 2, NDOT = 4;      // first-pass dot products
 constexpr int PREP_WARP0 = 6, NPREP = 2;    // cluster reduction, u and coef
-constexpr int EPI_WARP0 = 8, NEPI = 8;      // dx epilogue, then the dphi partial
+constexpr int EPI_WARP0 = 8, NEPI = 8;      // dx epilogue (4 warps per stream pair), then dphi
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t D1_COL = 0;              // one 64-column buffer per stream pair
 constexpr uint32_t D2_COL = 128;            // (chunk, pair) -> 32 columns
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
-constexpr bool LOOKAHEAD = true;            // first pass of tile j+1 before the second of j
 
-// Ring discipline: a wait on an mbarrier phase parity is only sound for a
-// waiter at most one phase behind, so every consumer walks every position of
-// a ring in order -- it waits for each box to land and arrives on its EMPTY
-// barrier, also for the boxes it does not read.  x boxes: the MMA thread (a
-// commit where it read the box), the four dot warps and the eight epilogue
-// warps (in the second pass the leader of each stream pair arrives for its
-// four warps once the pair's dx reduction has read the box); g_in boxes: the
-// dot and the epilogue warps.
-constexpr uint32_t XEMPTY_COUNT = 1 + NDOT + NEPI;
-constexpr uint32_t GEMPTY_COUNT = NDOT + NEPI;
+// Rings.  Every consumer of a ring visits each of its positions in order
+// (an mbarrier parity wait is only sound one phase behind):
+//   A: the four dot warps;
+//   B: the MMA thread (a commit: its products are done) and the leader of
+//      the position's stream pair (its dx reduction has read the box).  Pair
+//      p's positions fall in slots p and p + 2 only, so each pair also sees
+//      every phase of its own slots.
+constexpr uint32_t AEMPTY_COUNT = NDOT;
+constexpr uint32_t BEMPTY_COUNT = 2;
+static_assert(BSLOTS % 2 == 0, "each stream pair owns every other slot of ring B");
 
 enum : int {
-    BAR_XFULL = 0,
-    BAR_XEMPTY = BAR_XFULL + XSLOTS,
-    BAR_GFULL = BAR_XEMPTY + XSLOTS,
-    BAR_GEMPTY = BAR_GFULL + GSLOTS,
-    BAR_UFULL = BAR_GEMPTY + GSLOTS,
+    BAR_AFULL = 0,
+    BAR_AEMPTY = BAR_AFULL + ASLOTS,
+    BAR_BFULL = BAR_AEMPTY + ASLOTS,
+    BAR_BEMPTY = BAR_BFULL + BSLOTS,
+    BAR_UFULL = BAR_BEMPTY + BSLOTS,
     BAR_UEMPTY = BAR_UFULL + 1,
     BAR_D1FULL = BAR_UEMPTY + 1,
     BAR_D1EMPTY = BAR_D1FULL + 2,
@@ -116,27 +122,25 @@ enum : int {
 };
 
 struct Layout {
-    static constexpr uint32_t XR = 0;
-    static constexpr uint32_t GR = XR + XSLOTS * XBOX;
-    static constexpr uint32_t PHI = GR + GSLOTS * GBOX;
-    static constexpr uint32_t UA = PHI + 2 * MAX_NCK * PHI_BLK;    // 128 rows x 128 B
-    static constexpr uint32_t U2 = UA + 128 * 128;                  // 32 rows x 128 B
-    static constexpr uint32_t SC = U2 + 32 * 128;                   // per token: H_pre[4], coef
-    static constexpr uint32_t PART = SC + TT * 32;                  // [2][TT] float4
+    static constexpr uint32_t AR = 0;
+    static constexpr uint32_t BR = AR + ASLOTS * A_SLOT;
+    static constexpr uint32_t UA = BR + BSLOTS * B_SLOT;       // 128 rows x 128 B
+    static constexpr uint32_t U2 = UA + 128 * 128;             // 32 rows x 128 B
+    static constexpr uint32_t SC = U2 + 32 * 128;              // per token: H_pre[4], coef
+    static constexpr uint32_t PART = SC + TT * 32;             // [2][TT] float4
     static constexpr uint32_t BARS = PART + 2 * TT * 16;
     static constexpr uint32_t MISC = BARS + NBARS * 8;
     static constexpr uint32_t TOTAL = MISC + 64;
 };
 constexpr size_t SMEM_BYTES = Layout::TOTAL + 1024;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
-static_assert(Layout::PHI % 1024 == 0 && Layout::UA % 1024 == 0 && Layout::U2 % 1024 == 0, "alignment");
+static_assert(Layout::BR % 1024 == 0 && Layout::UA % 1024 == 0 && Layout::U2 % 1024 == 0, "alignment");
+static_assert(A_SLOT % 1024 == 0 && B_SLOT % 1024 == 0, "alignment");
 
 struct Params {
-    const float* phi;      // [K, 24]
     const float* proj;     // [T, 24]
     const float* alpha;    // [3]
     float* rec;            // [T, REC]
-    __nv_bfloat16* dx;     // [T, 4, D]
     float* part;           // [clusters, K, 24]
     int64_t T;
     int D;
@@ -164,37 +168,42 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     }
 }
 
-// Position in a ring of `n` slots: slot index and the parity of its use.
-struct Ring {
-    int slot = 0;
-    uint32_t phase = 0;
-    __device__ __forceinline__ void adv(int k, int n) {
-        slot += k;
-        while (slot >= n) {
-            slot -= n;
-            phase ^= 1u;
-        }
-    }
-};
-
-// Order of the passes: round r holds the first pass of tile p1(r) and then
-// the second pass of tile p2(r) (-1: none).  Every role walks the same
-// rounds, so that all agree on the ring positions.
-struct Sched {
-    int n;
-    __device__ int rounds() const { return LOOKAHEAD ? n + 1 : n; }
-    __device__ int p1(int r) const { return LOOKAHEAD ? (r < n ? r : -1) : r; }
-    __device__ int p2(int r) const { return LOOKAHEAD ? r - 1 : r; }
-};
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// PHI2 in global memory, rows of 64 bf16 (128 B, swizzled by TMA on load):
+// block (pair p, chunk q) holds, in row r, phi[(2p) D + 64q + r, 0..31] then
+// phi[(2p + 1) D + 64q + r, 0..31], logits 24..31 zero.
+__global__ void __launch_bounds__(256)
+pre_bwd_phi_pack_kernel(const float* __restrict__ phi, int64_t D, __nv_bfloat16* __restrict__ phi2) {
+    const int64_t nq = D / KC;
+    const int64_t items = 2 * nq * KC * 8;          // (pair, chunk, row, 16-byte piece)
+    for (int64_t it = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; it < items;
+         it += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int piece = static_cast<int>(it & 7);
+        const int64_t row = it >> 3;                // (p * nq + q) * 64 + r
+        const int r = static_cast<int>(row % KC);
+        const int64_t pq = row / KC;
+        const int p = static_cast<int>(pq / nq);
+        const int64_t q = pq % nq;
+        const int a = piece >> 2, g0 = (piece & 3) * 8;
+        const int64_t k = (2 * p + a) * D + q * KC + r;
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int g = g0 + 2 * e;
+            w[e] = pack_bf16x2(g < NG ? phi[k * NG + g] : 0.f, g + 1 < NG ? phi[k * NG + g + 1] : 0.f);
+        }
+        reinterpret_cast<uint4*>(phi2)[it] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
 __global__ void __launch_bounds__(NTHREADS, 1)
 pre_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dx,
-                     const __grid_constant__ CUtensorMap tm_g, const Params p) {
+                     const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_phi,
+                     const Params p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -211,21 +220,21 @@ pre_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
     const int ncl = static_cast<int>(ptx::nclusters_x());
     const int nck = p.nck;
     const int D = p.D;
+    const int nq = D / KC;                         // 64-column chunks per stream
     const int64_t K = 4 * static_cast<int64_t>(D);
-    const int d0 = static_cast<int>(rank) * nck * KC;
     const int ntl = p.ntiles > cl ? (p.ntiles - cl + ncl - 1) / ncl : 0;
-    const Sched sch{ntl};
     auto tile_t0 = [&](int jl) { return static_cast<int64_t>(cl + jl * ncl) * TT; };
+    auto chunk_col = [&](int c) { return (c * static_cast<int>(C) + static_cast<int>(rank)) * KC; };
 
     // ---- set-up ----------------------------------------------------------
     if (tid == 0) {
-        for (int s = 0; s < XSLOTS; ++s) {
-            ptx::mbar_init(bar(BAR_XFULL + s), 1);
-            ptx::mbar_init(bar(BAR_XEMPTY + s), XEMPTY_COUNT);
+        for (int s = 0; s < ASLOTS; ++s) {
+            ptx::mbar_init(bar(BAR_AFULL + s), 1);
+            ptx::mbar_init(bar(BAR_AEMPTY + s), AEMPTY_COUNT);
         }
-        for (int s = 0; s < GSLOTS; ++s) {
-            ptx::mbar_init(bar(BAR_GFULL + s), 1);
-            ptx::mbar_init(bar(BAR_GEMPTY + s), GEMPTY_COUNT);
+        for (int s = 0; s < BSLOTS; ++s) {
+            ptx::mbar_init(bar(BAR_BFULL + s), 1);
+            ptx::mbar_init(bar(BAR_BEMPTY + s), BEMPTY_COUNT);
         }
         ptx::mbar_init(bar(BAR_UFULL), NPREP * 32);
         ptx::mbar_init(bar(BAR_UEMPTY), 1 + NEPI);
@@ -243,27 +252,11 @@ pre_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
         ptx::prefetch_tmap(&tm_x);
         ptx::prefetch_tmap(&tm_dx);
         ptx::prefetch_tmap(&tm_g);
+        ptx::prefetch_tmap(&tm_phi);
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_slot), TMEM_COLS);
         ptx::tmem_relinquish();
-    }
-    // PHI2 block (chunk c, pair pp): row r, K-columns 32a .. 32a+31 hold
-    // bf16(phi[(2pp + a) D + d0 + 64c + r, g]) for g < 24, zero for g >= 24.
-    for (int item = tid; item < nck * 1024; item += NTHREADS) {
-        const int q = item & 3, a = (item >> 2) & 1, r = (item >> 3) & 63, blk = item >> 9;
-        const int c = blk >> 1, pp = blk & 1;
-        const int64_t k = static_cast<int64_t>(2 * pp + a) * D + d0 + c * KC + r;
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int g0 = q * 8 + 2 * e;
-            const float v0 = g0 < NG ? p.phi[k * NG + g0] : 0.f;
-            const float v1 = g0 + 1 < NG ? p.phi[k * NG + g0 + 1] : 0.f;
-            w[e] = pack_bf16x2(v0, v1);
-        }
-        *reinterpret_cast<uint4*>(smem + Layout::PHI + blk * PHI_BLK + ptx::sw128_off(r, a * 32 + q * 8)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
     }
     // U' and U start zero; the preparation warps only ever write their u parts.
     for (int i = tid; i < (128 * 128 + 32 * 128) / 16; i += NTHREADS)
@@ -277,109 +270,109 @@ pre_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer ----
+        // Positions of both rings run over (tile, chunk, stream pair).  Lane 0
+        // polls the two rings without blocking; a ring-B box is issued only
+        // after the ring-A box of the same position (so that it comes from
+        // L2), and ring A stays at most one tile ahead of ring B (so that the
+        // x and g_in it brings in are still in L2 for the second pass).
         const uint64_t keep = ptx::policy_evict_last();    // first pass: read again soon
         const uint64_t drop = ptx::policy_evict_first();   // second pass: last use
-        Ring X, G;
-        auto load_x = [&](const CUtensorMap* tm, int col, int64_t t0, uint64_t pol) -> bool {
-            bool ok = true;
-            if (lane == 0) ok = wait_bar(bar(BAR_XEMPTY + X.slot), X.phase ^ 1u, abort_flag);
-            if (!__shfl_sync(FULL, ok, 0)) return false;
+        const int npos = ntl * nck * 2;
+        int na = 0, nb = 0;
+        uint64_t idle_since = ptx::globaltimer();
+        while (na < npos || nb < npos) {
+            int moved = 0;
             if (lane == 0) {
-                const uint32_t fb = bar(BAR_XFULL + X.slot);
-                ptx::mbar_arrive_expect_tx(fb, XBOX);
-                ptx::tma_load_3d(sbase + Layout::XR + X.slot * XBOX, tm, col, static_cast<int>(t0), 0, fb, pol);
+                if (na < npos && na / (2 * nck) <= nb / (2 * nck) + 1) {
+                    const int slot = na % ASLOTS;
+                    if (ptx::mbar_test_wait(bar(BAR_AEMPTY + slot), ((na / ASLOTS) & 1) ^ 1)) {
+                        const int jl = na / (2 * nck), c = (na >> 1) % nck, pr = na & 1;
+                        const int64_t t0 = tile_t0(jl);
+                        const uint32_t dst = sbase + Layout::AR + slot * A_SLOT;
+                        const uint32_t fb = bar(BAR_AFULL + slot);
+                        ptx::mbar_arrive_expect_tx(fb, A_SLOT);
+                        ptx::tma_load_3d(dst, &tm_x, chunk_col(c), static_cast<int>(t0), 2 * pr, fb, keep);
+                        ptx::tma_load_2d(dst + PBOX, &tm_g, chunk_col(c), static_cast<int>(t0), fb, keep);
+                        ++na;
+                        moved = 1;
+                    }
+                }
+                if (nb < na) {
+                    const int slot = nb % BSLOTS;
+                    if (ptx::mbar_test_wait(bar(BAR_BEMPTY + slot), ((nb / BSLOTS) & 1) ^ 1)) {
+                        const int jl = nb / (2 * nck), c = (nb >> 1) % nck, pr = nb & 1;
+                        const int64_t t0 = tile_t0(jl);
+                        const uint32_t dst = sbase + Layout::BR + slot * B_SLOT;
+                        const uint32_t fb = bar(BAR_BFULL + slot);
+                        ptx::mbar_arrive_expect_tx(fb, B_SLOT);
+                        ptx::tma_load_3d(dst, &tm_x, chunk_col(c), static_cast<int>(t0), 2 * pr, fb, drop);
+                        ptx::tma_load_2d(dst + PBOX, &tm_phi, 0, (pr * nq + c * static_cast<int>(C) +
+                                                                   static_cast<int>(rank)) * KC, fb, keep);
+                        ptx::tma_load_2d(dst + PBOX + PHIB, &tm_g, chunk_col(c), static_cast<int>(t0), fb, drop);
+                        ++nb;
+                        moved = 1;
+                    }
+                }
+                if (moved) {
+                    idle_since = ptx::globaltimer();
+                } else if (*abort_flag) {
+                    moved = -1;
+                } else if (ptx::globaltimer() - idle_since > WAIT_LIMIT_NS) {
+                    atomicOr(&g_bwd_fused_error, 1u);
+                    *abort_flag = 1;
+                    moved = -1;
+                }
             }
-            __syncwarp();
-            X.adv(1, XSLOTS);
-            return true;
-        };
-        auto load_g = [&](int col, int64_t t0, uint64_t pol) -> bool {
-            bool ok = true;
-            if (lane == 0) ok = wait_bar(bar(BAR_GEMPTY + G.slot), G.phase ^ 1u, abort_flag);
-            if (!__shfl_sync(FULL, ok, 0)) return false;
-            if (lane == 0) {
-                const uint32_t fb = bar(BAR_GFULL + G.slot);
-                ptx::mbar_arrive_expect_tx(fb, GBOX);
-                ptx::tma_load_2d(sbase + Layout::GR + G.slot * GBOX, &tm_g, col, static_cast<int>(t0), fb, pol);
-            }
-            __syncwarp();
-            G.adv(1, GSLOTS);
-            return true;
-        };
-        for (int r = 0; r < sch.rounds(); ++r) {
-            const int a = sch.p1(r), b = sch.p2(r);
-            if (a >= 0) {
-                const int64_t t0 = tile_t0(a);
-                for (int c = 0; c < nck; ++c)
-                    if (!load_x(&tm_x, d0 + c * KC, t0, keep) || !load_g(d0 + c * KC, t0, keep)) goto done;
-            }
-            if (b >= 0) {
-                const int64_t t0 = tile_t0(b);
-                for (int c = 0; c < nck; ++c)
-                    if (!load_x(&tm_x, d0 + c * KC, t0, drop) || !load_g(d0 + c * KC, t0, drop)) goto done;
-            }
+            moved = __shfl_sync(FULL, moved, 0);
+            na = __shfl_sync(FULL, na, 0);
+            nb = __shfl_sync(FULL, nb, 0);
+            if (moved < 0) goto done;
         }
     } else if (warp == 1) {
         // ------------------------------------------------- MMA issuer -----
         constexpr uint32_t IDESC1 = ptx::idesc_bf16_f32(128, KC);               // D1: both K-major
         constexpr uint32_t IDESC2 = ptx::idesc_bf16_f32(128, 32) | (1u << 15);  // D2: A (x^T) MN-major
         // descriptors built once; the loop only moves their start address
-        const uint64_t desc_x0 = ptx::sw128_mnmajor_desc(sbase + Layout::XR, SUB, 1024);
+        const uint64_t desc_xmn = ptx::sw128_mnmajor_desc(sbase + Layout::BR, SUB, 1024);
+        const uint64_t desc_phi = ptx::sw128_kmajor_desc(sbase + Layout::BR + PBOX);
         const uint64_t desc_u2 = ptx::sw128_kmajor_desc(sbase + Layout::U2);
         const uint64_t desc_ua = ptx::sw128_kmajor_desc(sbase + Layout::UA);
-        const uint64_t desc_phi = ptx::sw128_kmajor_desc(sbase + Layout::PHI);
-        Ring X;
-        int s = 0, ju = 0;
-        // a box this thread does not read: wait for it, then release it
-        auto pass_x = [&]() -> bool {
-            bool ok = true;
-            if (lane == 0) {
-                ok = wait_bar(bar(BAR_XFULL + X.slot), X.phase, abort_flag);
-                if (ok) ptx::mbar_arrive(bar(BAR_XEMPTY + X.slot));
-            }
-            X.adv(1, XSLOTS);
-            return __shfl_sync(FULL, ok, 0);
-        };
-        for (int r = 0; r < sch.rounds(); ++r) {
-            if (sch.p1(r) >= 0)
-                for (int c = 0; c < nck; ++c)
-                    if (!pass_x()) goto done;
-            if (sch.p2(r) < 0) continue;
+        int s = 0;
+        for (int ju = 0; ju < ntl; ++ju) {
             bool ok = true;
             if (lane == 0) ok = wait_bar(bar(BAR_UFULL), ju & 1, abort_flag);
             if (!__shfl_sync(FULL, ok, 0)) goto done;
             for (int c = 0; c < nck; ++c, ++s) {
-                if (lane == 0) ok = wait_bar(bar(BAR_XFULL + X.slot), X.phase, abort_flag);
-                if (!__shfl_sync(FULL, ok, 0)) goto done;
                 for (int pp = 0; pp < 2; ++pp) {
-                    if (lane == 0) ok = wait_bar(bar(BAR_D1EMPTY + pp), (s & 1) ^ 1, abort_flag);
+                    const int n = (ju * nck + c) * 2 + pp;
+                    const int slot = n % BSLOTS;
+                    if (lane == 0)
+                        ok = wait_bar(bar(BAR_BFULL + slot), (n / BSLOTS) & 1, abort_flag) &&
+                             wait_bar(bar(BAR_D1EMPTY + pp), (s & 1) ^ 1, abort_flag);
                     if (!__shfl_sync(FULL, ok, 0)) goto done;
                     ptx::tc_fence_after();
                     if (lane == 0) {
                         // D2 first: the commit of D1FULL then also tells the pair's
-                        // epilogue that the MMA no longer reads its x sub-boxes,
-                        // which it overwrites with the dx increment
-                        const uint64_t dx2 = ptx::desc_add(desc_x0, X.slot * XBOX + pp * 2 * SUB);
+                        // epilogue that the MMA no longer reads the x box, which it
+                        // overwrites with the dx increment
+                        const uint64_t dx2 = ptx::desc_add(desc_xmn, slot * B_SLOT);
 #pragma unroll
                         for (int kk = 0; kk < TT / 16; ++kk)
                             ptx::tc_mma_f16(tmem + D2_COL + (c * 2 + pp) * 32, ptx::desc_add(dx2, kk * 2048),
                                             ptx::desc_add(desc_u2, kk * 32), IDESC2, (ju | kk) != 0);
-                        const uint64_t dphi = ptx::desc_add(desc_phi, (c * 2 + pp) * PHI_BLK);
+                        const uint64_t dphi = ptx::desc_add(desc_phi, slot * B_SLOT);
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
                             ptx::tc_mma_f16(tmem + D1_COL + pp * KC, ptx::desc_add(desc_ua, kk * 32),
                                             ptx::desc_add(dphi, kk * 32), IDESC1, kk != 0);
                         ptx::tc_commit(bar(BAR_D1FULL + pp));
+                        ptx::tc_commit(bar(BAR_BEMPTY + slot));
                     }
                     __syncwarp();
                 }
-                if (lane == 0) ptx::tc_commit(bar(BAR_XEMPTY + X.slot));
-                __syncwarp();
-                X.adv(1, XSLOTS);
             }
             if (lane == 0) ptx::tc_commit(bar(BAR_UEMPTY));
             __syncwarp();
-            ++ju;
         }
         if (lane == 0) ptx::tc_commit(bar(BAR_D2DONE));
         __syncwarp();
@@ -387,66 +380,46 @@ pre_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
         // -------------------------------------- first pass: dot products --
         const int q = tid - DOT_WARP0 * 32;            // 0..127
         const int t = q >> 1, h = q & 1;               // token, half of each chunk
-        Ring X, G;
-        int jd = 0;
-        for (int r = 0; r < sch.rounds(); ++r) {
-            if (sch.p1(r) >= 0) {
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                bool ok = true;
-                for (int c = 0; c < nck && ok; ++c) {
-                    ok = __all_sync(FULL, wait_bar(bar(BAR_XFULL + X.slot), X.phase, abort_flag)) &&
-                         __all_sync(FULL, wait_bar(bar(BAR_GFULL + G.slot), G.phase, abort_flag));
+        int n = 0;                                     // ring-A position
+        for (int jd = 0; jd < ntl; ++jd) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            bool ok = true;
+            for (int c = 0; c < nck && ok; ++c) {
+#pragma unroll
+                for (int pr = 0; pr < 2; ++pr, ++n) {
+                    const int slot = n % ASLOTS;
+                    ok = ok && __all_sync(FULL, wait_bar(bar(BAR_AFULL + slot), (n / ASLOTS) & 1, abort_flag));
                     if (!ok) break;
-                    const unsigned char* xb = smem + Layout::XR + X.slot * XBOX;
-                    const unsigned char* gb = smem + Layout::GR + G.slot * GBOX;
+                    const unsigned char* xb = smem + Layout::AR + slot * A_SLOT;
+                    const unsigned char* gb = xb + PBOX;
 #pragma unroll
                     for (int cq = 0; cq < 4; ++cq) {
                         const uint32_t off = static_cast<uint32_t>(t * 128 + (((h * 4 + cq) ^ (t & 7)) << 4));
                         float fg[8];
                         Vec<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(gb + off), fg);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
+                        for (int s2 = 0; s2 < 2; ++s2) {
                             float fx[8];
-                            Vec<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(xb + i * SUB + off), fx);
+                            Vec<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(xb + s2 * SUB + off), fx);
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) acc[i] = fmaf(fg[e], fx[e], acc[i]);
+                            for (int e = 0; e < 8; ++e) acc[2 * pr + s2] = fmaf(fg[e], fx[e], acc[2 * pr + s2]);
                         }
                     }
                     __syncwarp();
-                    if (lane == 0) {
-                        ptx::mbar_arrive(bar(BAR_XEMPTY + X.slot));
-                        ptx::mbar_arrive(bar(BAR_GEMPTY + G.slot));
-                    }
-                    X.adv(1, XSLOTS);
-                    G.adv(1, GSLOTS);
+                    if (lane == 0) ptx::mbar_arrive(bar(BAR_AEMPTY + slot));
                 }
-#pragma unroll
-                for (int i = 0; i < 4; ++i) acc[i] += __shfl_xor_sync(FULL, acc[i], 1);
-                const int ps = jd & 1;
-                if (ok) ok = __all_sync(FULL, wait_bar(bar(BAR_PEMPTY + ps), ((jd >> 1) & 1) ^ 1, abort_flag, true));
-                if (ok && h == 0)
-                    reinterpret_cast<float4*>(smem + Layout::PART + ps * TT * 16)[t] =
-                        make_float4(acc[0], acc[1], acc[2], acc[3]);
-                if (ptx::named_bar_or(1, NDOT * 32, !ok)) goto done;
-                if (warp == DOT_WARP0 && lane < static_cast<int>(C)) {
-                    ptx::fence_acq_rel_cluster();
-                    ptx::mbar_arrive_remote(ptx::mapa(bar(BAR_PFULL + ps), static_cast<uint32_t>(lane)));
-                }
-                ++jd;
             }
-            if (sch.p2(r) >= 0) {
-                // second-pass boxes (x, g_in per chunk): wait, release
-                bool ok = true;
-                for (int c = 0; c < nck && ok; ++c) {
-                    ok = __all_sync(FULL, wait_bar(bar(BAR_XFULL + X.slot), X.phase, abort_flag));
-                    if (ok && lane == 0) ptx::mbar_arrive(bar(BAR_XEMPTY + X.slot));
-                    X.adv(1, XSLOTS);
-                    if (!ok) break;
-                    ok = __all_sync(FULL, wait_bar(bar(BAR_GFULL + G.slot), G.phase, abort_flag));
-                    if (ok && lane == 0) ptx::mbar_arrive(bar(BAR_GEMPTY + G.slot));
-                    G.adv(1, GSLOTS);
-                }
-                if (ptx::named_bar_or(1, NDOT * 32, !ok)) goto done;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[i] += __shfl_xor_sync(FULL, acc[i], 1);
+            const int ps = jd & 1;
+            if (ok) ok = __all_sync(FULL, wait_bar(bar(BAR_PEMPTY + ps), ((jd >> 1) & 1) ^ 1, abort_flag, true));
+            if (ok && h == 0)
+                reinterpret_cast<float4*>(smem + Layout::PART + ps * TT * 16)[t] =
+                    make_float4(acc[0], acc[1], acc[2], acc[3]);
+            if (ptx::named_bar_or(1, NDOT * 32, !ok)) goto done;
+            if (warp == DOT_WARP0 && lane < static_cast<int>(C)) {
+                ptx::fence_acq_rel_cluster();
+                ptx::mbar_arrive_remote(ptx::mapa(bar(BAR_PFULL + ps), static_cast<uint32_t>(lane)));
             }
         }
     } else if (warp < EPI_WARP0) {
@@ -535,39 +508,10 @@ pre_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
         const int si = 2 * pp + (q >> 6);              // stream
         const int wq = warp & 3;                       // TMEM lane quarter of this warp
         const bool leader = q == 0;                    // issues the pair's dx reductions
-        Ring X, G;
-        int s = 0, ju = 0, pend = -1;                  // pend: x slot whose reduction may still read it
+        int s = 0;
         bool aborted = false;
-        // release the slot of the last reduction once the TMA has read it
-        auto flush = [&] {
-            if (leader && pend >= 0) {
-                ptx::bulk_wait_read<0>();
-                ptx::mbar_arrive_cnt(bar(BAR_XEMPTY + pend), 4);
-                pend = -1;
-            }
-        };
-        for (int r = 0; r < sch.rounds() && !aborted; ++r) {
-            if (sch.p1(r) >= 0) {
-                // first-pass boxes (x, g_in per chunk): wait, release
-                flush();
-                for (int c = 0; c < nck && !aborted; ++c) {
-                    if (!__all_sync(FULL, wait_bar(bar(BAR_XFULL + X.slot), X.phase, abort_flag)) ||
-                        !__all_sync(FULL, wait_bar(bar(BAR_GFULL + G.slot), G.phase, abort_flag))) {
-                        aborted = true;
-                        break;
-                    }
-                    if (lane == 0) {
-                        ptx::mbar_arrive(bar(BAR_XEMPTY + X.slot));
-                        ptx::mbar_arrive(bar(BAR_GEMPTY + G.slot));
-                    }
-                    X.adv(1, XSLOTS);
-                    G.adv(1, GSLOTS);
-                }
-                if (aborted) break;
-            }
-            const int b = sch.p2(r);
-            if (b < 0) continue;
-            const int t0 = static_cast<int>(tile_t0(b));
+        for (int ju = 0; ju < ntl && !aborted; ++ju) {
+            const int t0 = static_cast<int>(tile_t0(ju));
             // every thread of the pair passes the same named barriers, so a
             // failed wait is carried in `ok` and acted on at the barrier
             bool ok = __all_sync(FULL, wait_bar(bar(BAR_UFULL), ju & 1, abort_flag));
@@ -580,10 +524,12 @@ pre_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
                 if (lane == 0) ptx::mbar_arrive(bar(BAR_UEMPTY));
             }
             for (int c = 0; c < nck; ++c, ++s) {
+                const int n = (ju * nck + c) * 2 + pp;
+                const int slot = n % BSLOTS;
                 ok = ok && __all_sync(FULL, wait_bar(bar(BAR_D1FULL + pp), s & 1, abort_flag)) &&
-                     __all_sync(FULL, wait_bar(bar(BAR_XFULL + X.slot), X.phase, abort_flag)) &&
-                     __all_sync(FULL, wait_bar(bar(BAR_GFULL + G.slot), G.phase, abort_flag));
-                unsigned char* xb = smem + Layout::XR + X.slot * XBOX + si * SUB;
+                     __all_sync(FULL, wait_bar(bar(BAR_BFULL + slot), (n / BSLOTS) & 1, abort_flag));
+                unsigned char* box = smem + Layout::BR + slot * B_SLOT;
+                unsigned char* xb = box + (q >> 6) * SUB;
                 if (ok) {
                     ptx::tc_fence_after();
                     uint32_t v[4][16];
@@ -594,7 +540,7 @@ pre_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
                     ptx::tc_fence_before();
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(bar(BAR_D1EMPTY + pp));
-                    const unsigned char* gb = smem + Layout::GR + G.slot * GBOX;
+                    const unsigned char* gb = box + PBOX + PHIB;
                     // dx increment of this token and stream, written over the
                     // x row it was computed from (same swizzled place)
 #pragma unroll
@@ -617,26 +563,18 @@ pre_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
                     break;
                 }
                 if (leader) {
-                    // dx[t0.., 2pp..2pp+1, d0 + 64c ..] += the pair's two sub-boxes
-                    ptx::tma_reduce_add_3d(&tm_dx, d0 + c * KC, t0, 2 * pp,
-                                           sbase + Layout::XR + X.slot * XBOX + pp * 2 * SUB);
+                    // dx[t0.., 2pp..2pp+1, chunk] += the pair's box; the slot is
+                    // free once the reduction has read it
+                    ptx::tma_reduce_add_3d(&tm_dx, chunk_col(c), t0, 2 * pp, sbase + Layout::BR + slot * B_SLOT);
                     ptx::bulk_commit();
-                    ptx::mbar_arrive_cnt(bar(BAR_GEMPTY + G.slot), 4);
-                    if (pend >= 0) {
-                        ptx::bulk_wait_read<1>();
-                        ptx::mbar_arrive_cnt(bar(BAR_XEMPTY + pend), 4);
-                    }
-                    pend = X.slot;
+                    ptx::bulk_wait_read<0>();
+                    ptx::mbar_arrive(bar(BAR_BEMPTY + slot));
                 }
-                X.adv(1, XSLOTS);
-                G.adv(1, GSLOTS);
             }
-            ++ju;
         }
-        flush();
         if (leader) ptx::bulk_wait<0>();   // the reductions are complete before the kernel ends
         // dphi partial of this cluster: D2 row q of (chunk c, pair pp) is
-        // column k = si * D + d0 + 64c + t.
+        // column k = si * D + 64 (c C + rank) + t.
         if (!aborted && __all_sync(FULL, wait_bar(bar(BAR_D2DONE), 0, abort_flag))) {
             ptx::tc_fence_after();
             float* out = p.part + static_cast<int64_t>(cl) * K * NG;
@@ -646,8 +584,8 @@ pre_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
                 ptx::tmem_ld16(ta, w0);
                 ptx::tmem_ld16(ta + 16, w1);
                 ptx::tmem_wait_ld();
-                float4* o4 = reinterpret_cast<float4*>(out + (static_cast<int64_t>(si) * D + d0 + c * KC + t) * NG);
-                const bool any = ju > 0;
+                float4* o4 = reinterpret_cast<float4*>(out + (static_cast<int64_t>(si) * D + chunk_col(c) + t) * NG);
+                const bool any = ntl > 0;
 #pragma unroll
                 for (int v4 = 0; v4 < 4; ++v4)
                     o4[v4] = any ? make_float4(__uint_as_float(w0[4 * v4]), __uint_as_float(w0[4 * v4 + 1]),
@@ -676,8 +614,8 @@ done:
     ptx::cluster_sync();   // no CTA leaves while a peer may still touch its shared memory
 }
 
-// Smallest cluster whose per-CTA column slice is a whole number of 64-column
-// chunks, at most MAX_NCK of them (phi slice and dphi accumulators on chip).
+// Smallest cluster whose per-CTA share is a whole number of 64-column chunks
+// per stream, at most MAX_NCK of them (dphi accumulators in TMEM).
 int cluster_for(int64_t D) {
     if (D <= 0 || D % KC != 0) return 0;
     const int64_t nc = D / KC;
@@ -734,21 +672,22 @@ int max_clusters(int C) {
 }
 
 // dims (d, t, stream) of a [T, 4, D] tensor: box = 64 columns x 64 tokens x
-// `streams` streams, laid out in shared memory as [stream][token][64 columns]
-bool encode_x(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* tm, const void* base, int64_t T, int64_t D,
-              int streams) {
+// 2 streams, laid out in shared memory as [stream][token][64 columns]
+bool encode_x(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* tm, const void* base, int64_t T, int64_t D) {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(T), 4};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(8 * D), static_cast<cuuint64_t>(2 * D)};
-    const cuuint32_t box[3] = {KC, TT, static_cast<cuuint32_t>(streams)};
+    const cuuint32_t box[3] = {KC, TT, 2};
     const cuuint32_t estr[3] = {1, 1, 1};
     return encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool encode_g(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* tm, const void* base, int64_t T, int64_t D) {
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(T)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(2 * D)};
+// A [rows, inner] bf16 matrix read in boxes of 64 x 64.
+bool encode_2d(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* tm, const void* base, int64_t inner,
+               int64_t rows) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(2 * inner)};
     const cuuint32_t box[2] = {KC, TT};
     const cuuint32_t estr[2] = {1, 1};
     return encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
@@ -764,24 +703,28 @@ bool pre_bwd_fused_supports(int64_t T, int64_t D) {
     return C > 0 && tensor_map_encoder() != nullptr && bwdfu::max_clusters(C) > 0;
 }
 
+size_t pre_bwd_fused_phi_bytes(int64_t D) { return static_cast<size_t>(D) * 256; }
+
 cudaError_t launch_pre_bwd_fused_main(const void* g_in, const void* x, const float* phi,
                                       const float* proj, const float* alpha, float* rec,
                                       int64_t T, int64_t D, int64_t max_parts, void* dx,
-                                      float* part, int64_t* nparts, cudaStream_t s) {
+                                      float* part, void* phi2, int64_t* nparts, cudaStream_t s) {
     auto encode = tensor_map_encoder();
     const int C = bwdfu::cluster_for(D);
     if (encode == nullptr || C == 0 || !bwdfu::set_attributes_once()) return cudaErrorNotSupported;
-    CUtensorMap tx, tdx, tg;
-    // x is read as 4-stream boxes; dx only receives reductions of 2-stream boxes
-    if (!bwdfu::encode_x(encode, &tx, x, T, D, 4) || !bwdfu::encode_x(encode, &tdx, dx, T, D, 2) ||
-        !bwdfu::encode_g(encode, &tg, g_in, T, D))
+    CUtensorMap tx, tdx, tg, tphi;
+    if (!bwdfu::encode_x(encode, &tx, x, T, D) || !bwdfu::encode_x(encode, &tdx, dx, T, D) ||
+        !bwdfu::encode_2d(encode, &tg, g_in, D, T) || !bwdfu::encode_2d(encode, &tphi, phi2, bwdfu::KC, 2 * D))
         return cudaErrorInvalidValue;
+    // phi as bf16 pair blocks for the second pass (read from L2 by TMA)
+    const int64_t pack_items = 2 * (D / bwdfu::KC) * bwdfu::KC * 8;
+    const int64_t pack_blocks = (pack_items + 255) / 256;
+    bwdfu::pre_bwd_phi_pack_kernel<<<static_cast<unsigned>(pack_blocks < 1024 ? pack_blocks : 1024), 256, 0, s>>>(
+        phi, D, static_cast<__nv_bfloat16*>(phi2));
     bwdfu::Params prm;
-    prm.phi = phi;
     prm.proj = proj;
     prm.alpha = alpha;
     prm.rec = rec;
-    prm.dx = static_cast<__nv_bfloat16*>(dx);
     prm.part = part;
     prm.T = T;
     prm.D = static_cast<int>(D);
@@ -794,7 +737,7 @@ cudaError_t launch_pre_bwd_fused_main(const void* g_in, const void* x, const flo
     *nparts = ncl;
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = bwdfu::config(C, static_cast<int>(ncl), s, attr);
-    return cudaLaunchKernelEx(&cfg, bwdfu::pre_bwd_fused_kernel, tx, tdx, tg, prm);
+    return cudaLaunchKernelEx(&cfg, bwdfu::pre_bwd_fused_kernel, tx, tdx, tg, tphi, prm);
 }
 
 }  // namespace mhc

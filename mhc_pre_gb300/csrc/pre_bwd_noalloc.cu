@@ -73,14 +73,16 @@ extern "C" mhc_status mhc_pre_bwd_noalloc(mhc_dtype dt, const void* g_in, const 
         if (p == nullptr) return MHC_ERR_INVALID_ARG;
         if (!mhc::aligned16(p)) return MHC_ERR_MISALIGNED;
     }
-    // Scratch plan: T per-token records, then as many dphi token blocks as
-    // both the usual plan and the fixed array allow (at least one).
+    // Scratch plan: T per-token records, as many dphi token blocks as both the
+    // usual plan and the fixed array allow (at least one), then the bf16 phi
+    // blocks of the one-pass kernel.
     const size_t rec_bytes = static_cast<size_t>(T) * mhc::REC * sizeof(float);
     const size_t part_bytes = static_cast<size_t>(4 * D) * mhc::kLogits * sizeof(float);
+    const size_t phi_bytes = mhc::pre_bwd_fused_phi_bytes(D);
     const size_t cap = MHC_PRE_BWD_NOALLOC_SCRATCH_BYTES;
-    if (rec_bytes + part_bytes > cap) return MHC_ERR_UNSUPPORTED;   // too large for the array
+    if (rec_bytes + part_bytes + phi_bytes > cap) return MHC_ERR_UNSUPPORTED;   // too large for the array
     int64_t nb = mhc::pre_bwd_plan(T, D).nb;
-    const int64_t fit = static_cast<int64_t>((cap - rec_bytes) / part_bytes);
+    const int64_t fit = static_cast<int64_t>((cap - rec_bytes - phi_bytes) / part_bytes);
     if (nb > fit) nb = fit;
     void* ws = mhc::scratch_on_current_device();
     if (ws == nullptr) return MHC_ERR_CUDA;

@@ -128,8 +128,8 @@ def test_missing_library_fails_loudly(tmp_path):
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(L):
-    # 16 MiB of scratch: T * 256 B of records plus one 4*D x 24 float partial
-    # must fit; the refusal comes before any CUDA call.
+    # 16 MiB of scratch: T * 256 B of records, one 4*D x 24 float partial and
+    # D * 256 B of bf16 phi blocks must fit; the refusal comes before any CUDA call.
     args = [A] * 9
 
     def call(T, D):
