@@ -217,8 +217,9 @@ def main():
     mbuild.build()
 
     w = W.WORKLOADS[args.workload].with_(iters=args.iters, backward=True)
-    if args.tokens is not None:
-        w = w.with_(T=args.tokens)
+    if args.tokens is not None and args.tokens != w.T:
+        # a smaller case of the same shape, for profiling; the name says so
+        w = w.with_(T=args.tokens, name=f"{w.name}, T overridden to {args.tokens}")
     inp = W.make_inputs(w, device=dev, seed=1000 + w.wid + 7919 * rank)
     ws = torch.empty((max(B.pre_bwd_workspace_bytes(torch.bfloat16, w.T, w.n, w.D), 16),),
                      dtype=torch.uint8, device=dev)
