@@ -192,7 +192,9 @@ pre_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer ----
-        const uint64_t pol = ptx::policy_evict_last();
+        // normal priority: evict-last lines outlive the kernel and crowd the
+        // next kernel's working set out of L2
+        const uint64_t pol = ptx::policy_evict_normal();
         int stage = 0;
         uint32_t round = 0;
         for (int j = 0; j < ntiles; ++j) {
