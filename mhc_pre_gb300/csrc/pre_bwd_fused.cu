@@ -409,6 +409,8 @@ pre_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
                             for (int e = 0; e < 8; ++e) acc[2 * pr + s2] = fmaf(fg[e], fx[e], acc[2 * pr + s2]);
                         }
                     }
+                    // the slot's next bytes come through the async proxy (TMA)
+                    ptx::fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(bar(BAR_AEMPTY + slot));
                 }

@@ -351,6 +351,8 @@ pre_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
                     ds4[cq] = *reinterpret_cast<const uint4*>(st + ARR_BYTES + off);
                     gs4[cq] = *reinterpret_cast<const uint4*>(st + 2 * ARR_BYTES + off);
                 }
+                // the stage's next bytes come through the async proxy (TMA)
+                ptx::fence_proxy_async_smem();
                 ptx::mbar_arrive(bar(BAR_EMPTY + stage));
                 if (t < tend) {
                     __nv_bfloat16* dst = p.dx + t * K + kbase + c * KC + half * 32;

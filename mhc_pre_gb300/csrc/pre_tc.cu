@@ -433,7 +433,9 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
                 }
             }
             // every gate warp is done with the records: arm the barrier for the
-            // next tile's, then tell every sender the buffer is free
+            // next tile's, then tell every sender the buffer is free (peers
+            // refill it with st.async)
+            ptx::fence_proxy_async_smem();
             if (ptx::named_bar_or(1, NGATE * 32, !ok)) break;
             if (warp == GATE_WARP0) {
                 if (lane == 0) ptx::mbar_arrive(bar(BAR_SKFULL + tb));
@@ -544,7 +546,9 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
                 }
             }
             // every mix thread is done with this parity's H_pre: arm it for
-            // tile it + 2, then free it at every reducer
+            // tile it + 2, then free it at every reducer (which refills it
+            // with st.async)
+            ptx::fence_proxy_async_smem();
             if (ptx::named_bar_or(3, NMIX * 32, !ok)) break;
             if (warp == MIX_WARP0) {
                 if (lane == 0 && it + 2 < ntl) ptx::mbar_arrive_expect_tx(bar(BAR_HPRE + tb), TILE_M * 16);
