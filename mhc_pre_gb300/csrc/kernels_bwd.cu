@@ -133,6 +133,9 @@ pre_bwd_token_kernel(const float* __restrict__ dH_post, const float* __restrict_
                      const float* __restrict__ b, const float* __restrict__ alpha,
                      const float* __restrict__ proj, const float* __restrict__ inv_rms, int64_t T,
                      int64_t K, int iters, int have_dhpre, float* __restrict__ rec) {
+    // a programmatically dependent kernel after this one may start now; it
+    // waits for this kernel's completion before reading the records
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (t >= T) return;
     float* r = rec + t * REC;
@@ -374,10 +377,13 @@ void set_main_smem_once() {
     }
 }
 
+constexpr int BIAS_W = 28;          // bias partial: dlogits[24], da[3], one unused float
+
 // 4a. dphi = sum over token blocks of the partials (fixed order).
 __global__ void __launch_bounds__(256)
 pre_bwd_reduce_phi_kernel(const float* __restrict__ part, int64_t nb, int64_t n4,
-                          float* __restrict__ dphi) {
+                          float* __restrict__ dphi, const float* __restrict__ bpart, int nbb,
+                          float* __restrict__ db, float* __restrict__ dalpha) {
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         float4 s = reinterpret_cast<const float4*>(part)[i];
@@ -387,28 +393,55 @@ pre_bwd_reduce_phi_kernel(const float* __restrict__ part, int64_t nb, int64_t n4
         }
         reinterpret_cast<float4*>(dphi)[i] = s;
     }
+    // db and dalpha: the bias partials of every token block, in block order
+    if (blockIdx.x == 0 && threadIdx.x < NG + 3) {
+        float tot = 0.f;
+        for (int b = 0; b < nbb; ++b) tot += bpart[b * BIAS_W + threadIdx.x];
+        if (threadIdx.x < NG) db[threadIdx.x] = tot;
+        else dalpha[threadIdx.x - NG] = tot;
+    }
 }
 
-// 4b. db[g] = sum_t dlogits[t, g]; dalpha[c] = sum_t da[t, c].  One CTA per
-//     output column; each thread sums a strided subset of tokens, then a
-//     fixed-shape tree over the CTA (deterministic).
+// 4b. db[g] = sum_t dlogits[t, g] and dalpha[c] = sum_t da[t, c], in two
+//     deterministic steps.  Here, block b sums its contiguous token range:
+//     a warp reads four tokens' 28 floats (dlogits[24], da[3], one unused)
+//     at a time as float4 pieces, lanes 7k + v holding piece v of token k;
+//     then a fixed-shape tree over the lanes and the warps.  The per-block
+//     partials [nbb][28] are summed in order by block 0 of the dphi reduction.
 __global__ void __launch_bounds__(256)
-pre_bwd_reduce_bias_kernel(const float* __restrict__ rec, int64_t T, float* __restrict__ db,
-                           float* __restrict__ dalpha) {
-    __shared__ float part_s[256 / 32];
-    const int col = blockIdx.x;
-    const int off = col < NG ? REC_DL + col : REC_DA + (col - NG);
-    float s = 0.f;
-    for (int64_t t = threadIdx.x; t < T; t += 256) s += rec[t * REC + off];
-    s = warp_sum(s);
-    if ((threadIdx.x & 31) == 0) part_s[threadIdx.x >> 5] = s;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float tot = 0.f;
+pre_bwd_bias_partial_kernel(const float* __restrict__ rec, int64_t T, float* __restrict__ bpart) {
+    __shared__ float4 wsum[8][BIAS_W / 4];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t per = (T + gridDim.x - 1) / gridDim.x;
+    const int64_t t_begin = static_cast<int64_t>(blockIdx.x) * per;
+    const int64_t t_end = t_begin + per < T ? t_begin + per : T;
+    const int k = lane / 7, v = lane - 7 * (lane / 7);   // token slot, piece
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lane < 28) {
+        for (int64_t t = t_begin + warp * 4 + k; t < t_end; t += 32) {
+            const float4 a = reinterpret_cast<const float4*>(rec + t * REC + REC_DL)[v];
+            acc.x += a.x; acc.y += a.y; acc.z += a.z; acc.w += a.w;
+        }
+    }
+    // lanes v, v + 7, v + 14, v + 21 hold piece v of the four token slots
 #pragma unroll
-        for (int w = 0; w < 256 / 32; ++w) tot += part_s[w];
-        if (col < NG) db[col] = tot;
-        else dalpha[col - NG] = tot;
+    for (int j = 1; j < 4; ++j) {
+        const float x = __shfl_sync(0xffffffffu, acc.x, (lane + 7 * j) & 31);
+        const float y = __shfl_sync(0xffffffffu, acc.y, (lane + 7 * j) & 31);
+        const float z = __shfl_sync(0xffffffffu, acc.z, (lane + 7 * j) & 31);
+        const float w = __shfl_sync(0xffffffffu, acc.w, (lane + 7 * j) & 31);
+        if (lane < 7) { acc.x += x; acc.y += y; acc.z += z; acc.w += w; }
+    }
+    if (lane < 7) wsum[warp][lane] = acc;
+    __syncthreads();
+    if (threadIdx.x < BIAS_W / 4) {
+        float4 tot = wsum[0][threadIdx.x];
+#pragma unroll
+        for (int w2 = 1; w2 < 8; ++w2) {
+            const float4 a = wsum[w2][threadIdx.x];
+            tot.x += a.x; tot.y += a.y; tot.z += a.z; tot.w += a.w;
+        }
+        reinterpret_cast<float4*>(bpart + static_cast<int64_t>(blockIdx.x) * BIAS_W)[threadIdx.x] = tot;
     }
 }
 
@@ -465,11 +498,15 @@ cudaError_t launch_pre_bwd_blocks(bool bf16, const void* g_in, const float* dH_p
     const dim3 gm(static_cast<unsigned>((K + MB_KS - 1) / MB_KS), static_cast<unsigned>(nb));
     int64_t nparts = nb;
     if (bf16 && pre_bwd_fused_supports(T, D)) {
-        // one pass: per-token gate backward first (it does not need dH_pre),
-        // then the cluster kernel finds dH_pre and does the rest
-        pre_bwd_token_kernel<<<gt, 128, 0, s>>>(dH_post, dH_res, b, alpha, proj, inv_rms, T, K, iters, 0, rec);
+        // one pass: phi packed for the cluster kernel, the per-token gate
+        // backward (it does not need dH_pre), then the cluster kernel finds
+        // dH_pre and does the rest; it starts while the per-token kernel
+        // finishes and waits for its records only where it reads them
         void* phi2 = static_cast<char*>(ws) + static_cast<size_t>(T) * REC * sizeof(float) +
                      static_cast<size_t>(nb) * K * NG * sizeof(float);
+        const cudaError_t ep = launch_pre_bwd_phi_pack(phi, D, phi2, s);
+        if (ep != cudaSuccess) return ep;
+        pre_bwd_token_kernel<<<gt, 128, 0, s>>>(dH_post, dH_res, b, alpha, proj, inv_rms, T, K, iters, 0, rec);
         const cudaError_t e = launch_pre_bwd_fused_main(g_in, x, phi, proj, alpha, rec, T, D, nb, dx, part,
                                                         phi2, &nparts, s);
         if (e != cudaSuccess) return e;
@@ -497,8 +534,17 @@ cudaError_t launch_pre_bwd_blocks(bool bf16, const void* g_in, const float* dH_p
     }
     const int64_t n4 = K * NG / 4;
     const dim3 gr(static_cast<unsigned>((n4 + 255) / 256 < 4096 ? (n4 + 255) / 256 : 4096));
-    pre_bwd_reduce_phi_kernel<<<gr, 256, 0, s>>>(part, nparts, n4, dphi);
-    pre_bwd_reduce_bias_kernel<<<NG + 3, 256, 0, s>>>(rec, T, db, dalpha);
+    // the bias partials go where the bf16 phi blocks were (dead once the
+    // main kernel is done; the region is reserved on every path)
+    float* bpart = reinterpret_cast<float*>(static_cast<char*>(ws) + static_cast<size_t>(T) * REC * sizeof(float) +
+                                            static_cast<size_t>(nb) * K * NG * sizeof(float));
+    int64_t nbb = (T + 255) / 256;
+    const int64_t fit = static_cast<int64_t>(pre_bwd_fused_phi_bytes(D) / (BIAS_W * sizeof(float)));
+    if (nbb > 128) nbb = 128;
+    if (nbb > fit) nbb = fit;
+    if (nbb < 1) nbb = 1;
+    pre_bwd_bias_partial_kernel<<<static_cast<unsigned>(nbb), 256, 0, s>>>(rec, T, bpart);
+    pre_bwd_reduce_phi_kernel<<<gr, 256, 0, s>>>(part, nparts, n4, dphi, bpart, static_cast<int>(nbb), db, dalpha);
     return cudaGetLastError();
 }
 

@@ -66,6 +66,8 @@ cudaError_t launch_pre_bwd_blocks(bool bf16, const void* g_in, const float* dH_p
 // It first packs phi as bf16 pair blocks into `phi2` (pre_bwd_fused_phi_bytes).
 bool pre_bwd_fused_supports(int64_t T, int64_t D);
 size_t pre_bwd_fused_phi_bytes(int64_t D);
+// bf16 phi blocks of the one-pass kernel, packed into the workspace.
+cudaError_t launch_pre_bwd_phi_pack(const float* phi, int64_t D, void* phi2, cudaStream_t s);
 cudaError_t launch_pre_bwd_fused_main(const void* g_in, const void* x, const float* phi,
                                       const float* proj, const float* alpha, float* rec,
                                       int64_t T, int64_t D, int64_t max_parts, void* dx,

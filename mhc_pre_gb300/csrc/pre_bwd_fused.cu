@@ -431,6 +431,9 @@ pre_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
     } else if (warp < EPI_WARP0) {
         // ------------------------------ cluster reduction, u and coef -----
         const int t = tid - PREP_WARP0 * 32;           // 0..63: token of the tile
+        // the per-token kernel before this one (which may still be running:
+        // programmatic dependent launch) wrote the records read below
+        ptx::griddep_wait();
         const float apre = p.alpha[0];
         const float invK = 1.0f / static_cast<float>(K);
         for (int jl = 0; jl < ntl; ++jl) {
@@ -722,11 +725,8 @@ cudaError_t launch_pre_bwd_fused_main(const void* g_in, const void* x, const flo
     if (!bwdfu::encode_x(encode, &tx, x, T, D) || !bwdfu::encode_x(encode, &tdx, dx, T, D) ||
         !bwdfu::encode_2d(encode, &tg, g_in, D, T) || !bwdfu::encode_2d(encode, &tphi, phi2, bwdfu::KC, 2 * D))
         return cudaErrorInvalidValue;
-    // phi as bf16 pair blocks for the second pass (read from L2 by TMA)
-    const int64_t pack_items = 2 * (D / bwdfu::KC) * bwdfu::KC * 8;
-    const int64_t pack_blocks = (pack_items + 255) / 256;
-    bwdfu::pre_bwd_phi_pack_kernel<<<static_cast<unsigned>(pack_blocks < 1024 ? pack_blocks : 1024), 256, 0, s>>>(
-        phi, D, static_cast<__nv_bfloat16*>(phi2));
+    (void)phi;
+    (void)phi2;
     bwdfu::Params prm;
     prm.proj = proj;
     prm.alpha = alpha;
@@ -741,9 +741,24 @@ cudaError_t launch_pre_bwd_fused_main(const void* g_in, const void* x, const flo
     if (ncl > max_parts) ncl = max_parts;
     if (ncl <= 0) return cudaErrorNotSupported;
     *nparts = ncl;
-    cudaLaunchAttribute attr[1];
-    const cudaLaunchConfig_t cfg = bwdfu::config(C, static_cast<int>(ncl), s, attr);
+    // Programmatic dependent launch: the kernel may start while the
+    // per-token kernel before it finishes; only the reduction warps need that
+    // kernel's records, and they wait for it (griddepcontrol.wait).
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = bwdfu::config(C, static_cast<int>(ncl), s, attr);
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, bwdfu::pre_bwd_fused_kernel, tx, tdx, tg, tphi, prm);
+}
+
+cudaError_t launch_pre_bwd_phi_pack(const float* phi, int64_t D, void* phi2, cudaStream_t s) {
+    // phi as bf16 pair blocks for the second pass (read from L2 by TMA)
+    const int64_t pack_items = 2 * (D / bwdfu::KC) * bwdfu::KC * 8;
+    const int64_t pack_blocks = (pack_items + 255) / 256;
+    bwdfu::pre_bwd_phi_pack_kernel<<<static_cast<unsigned>(pack_blocks < 1024 ? pack_blocks : 1024), 256, 0, s>>>(
+        phi, D, static_cast<__nv_bfloat16*>(phi2));
+    return cudaGetLastError();
 }
 
 }  // namespace mhc
