@@ -94,6 +94,7 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t D1_COL = 0;              // one 64-column buffer per stream pair
 constexpr uint32_t D2_COL = 128;            // (chunk, pair) -> 32 columns
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
+constexpr int AHEAD = 2;                    // tiles the first pass may run ahead of the second
 
 // Rings.  Every consumer of a ring visits each of its positions in order
 // (an mbarrier parity wait is only sound one phase behind):
@@ -273,8 +274,9 @@ pre_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
         // Positions of both rings run over (tile, chunk, stream pair).  Lane 0
         // polls the two rings without blocking; a ring-B box is issued only
         // after the ring-A box of the same position (so that it comes from
-        // L2), and ring A stays at most one tile ahead of ring B (so that the
-        // x and g_in it brings in are still in L2 for the second pass).
+        // L2), and ring A stays at most AHEAD tiles ahead of ring B (so that
+        // the x and g_in it brings in are still in L2 for the second pass:
+        // two tiles of every cluster are about 45 MB).
         // First pass: normal priority.  An evict-last hint would keep the
         // boxes for the second pass no better (it comes one tile later) and
         // the lines keep that priority after the kernel ends: the next
@@ -287,7 +289,7 @@ pre_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
         while (na < npos || nb < npos) {
             int moved = 0;
             if (lane == 0) {
-                if (na < npos && na / (2 * nck) <= nb / (2 * nck) + 1) {
+                if (na < npos && na / (2 * nck) <= nb / (2 * nck) + AHEAD) {
                     const int slot = na % ASLOTS;
                     if (ptx::mbar_test_wait(bar(BAR_AEMPTY + slot), ((na / ASLOTS) & 1) ^ 1)) {
                         const int jl = na / (2 * nck), c = (na >> 1) % nck, pr = na & 1;
