@@ -91,6 +91,7 @@ constexpr int GATE_WARP0 = 2, NGATE = 4;          // TMEM readers, cluster reduc
 constexpr int SK_WARP = 6;                        // Sinkhorn, other gates, outputs
 constexpr int MIX_WARP0 = 7, NMIX = 9;            // x_in = sum_i H_pre[i] x[i]
 constexpr int SKF = 28;                           // hand-off record: proj[24], inv_rms (floats)
+constexpr int NHP = 4;                            // H_pre buffers: tiles between reducers and mixes
 constexpr int REC = 25;                           // partial record: 24 logits + sum x^2
 constexpr int RB = 28;                            // its stride in floats (16-byte aligned)
 constexpr uint32_t REC_TX = REC * 4;              // bytes of one record pushed to its reducer
@@ -112,9 +113,9 @@ enum : int {
     BAR_ACC_EMPTY = BAR_ACC_FULL + 2,
     BAR_RECV = BAR_ACC_EMPTY + 2,    // this CTA's tokens: every peer's partial record arrived
     BAR_RFREE = BAR_RECV + 1,       // every reducer of the cluster has read the last tile's records
-    BAR_HPRE = BAR_RFREE + 1,       // [2] H_pre of the tile parity arrived from the reducers
-    BAR_HFREE = BAR_HPRE + 2,       // [2] every CTA's mix has finished with that parity
-    BAR_SKFULL = BAR_HFREE + 2,     // [2] reduced tokens handed to the Sinkhorn warp
+    BAR_HPRE = BAR_RFREE + 1,       // [NHP] H_pre of tile it (buffer it % NHP) arrived from the reducers
+    BAR_HFREE = BAR_HPRE + NHP,     // [NHP] every CTA's mix has finished with that buffer
+    BAR_SKFULL = BAR_HFREE + NHP,   // [2] reduced tokens handed to the Sinkhorn warp
     BAR_SKEMPTY = BAR_SKFULL + 2,   // [2] the Sinkhorn warp is done with them
     NBARS = BAR_SKEMPTY + 2
 };
@@ -128,7 +129,7 @@ struct Layout {
         L.stages = static_cast<uint32_t>(nch) * PHI_CHUNK_BYTES;   // multiple of 1024
         L.recv = L.stages + STAGES * STAGE_BYTES;    // [C senders][TILE_M / C tokens][2 halves][RB]
         L.hpre = L.recv + 2 * TILE_M * RB * 4;
-        L.sk = L.hpre + 2 * TILE_M * 16;              // [2][tpc][SKF]
+        L.sk = L.hpre + NHP * TILE_M * 16;            // [2][tpc][SKF]
         L.bars = L.sk + 2 * tpc * SKF * 4;
         L.misc = L.bars + NBARS * 8;
         L.total = L.misc + 64 + 32 * 4;   // tmem slot, abort flag, alpha, b
@@ -207,8 +208,6 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(bar(BAR_ACC_FULL + i), 1);
             ptx::mbar_init(bar(BAR_ACC_EMPTY + i), 128);
-            ptx::mbar_init(bar(BAR_HPRE + i), 1);
-            ptx::mbar_init(bar(BAR_HFREE + i), C);
             ptx::mbar_init(bar(BAR_SKFULL + i), 1);
             ptx::mbar_init(bar(BAR_SKEMPTY + i), 1);
         }
@@ -217,8 +216,11 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
         // receive barriers are armed one use ahead, before any peer can send:
         // records of the first tile, H_pre of the first two
         if (ntl > 0) ptx::mbar_arrive_expect_tx(bar(BAR_RECV), 2 * TILE_M * REC_TX);
-        if (ntl > 0) ptx::mbar_arrive_expect_tx(bar(BAR_HPRE + 0), TILE_M * 16);
-        if (ntl > 1) ptx::mbar_arrive_expect_tx(bar(BAR_HPRE + 1), TILE_M * 16);
+        for (int i = 0; i < NHP; ++i) {
+            ptx::mbar_init(bar(BAR_HPRE + i), 1);
+            ptx::mbar_init(bar(BAR_HFREE + i), C);
+            if (i < ntl) ptx::mbar_arrive_expect_tx(bar(BAR_HPRE + i), TILE_M * 16);
+        }
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -383,8 +385,10 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
                                      recv_bar);
                 ptx::st_async_b32(rec_dst + 4 * NG, ssv, recv_bar);
             }
-            // H_pre of this parity is free at every CTA (mix of tile it-2 done)
-            if (it >= 2) ok = ok && __all_sync(FULL, wait_bar<true>(bar(BAR_HFREE + tb), (use - 1) & 1, abort_flag));
+            // H_pre buffer it % NHP is free at every CTA (mix of tile it - NHP done)
+            const int hs = it % NHP;
+            if (it >= NHP)
+                ok = ok && __all_sync(FULL, wait_bar<true>(bar(BAR_HFREE + hs), ((it / NHP) - 1) & 1, abort_flag));
             // the Sinkhorn warp is done with this parity's hand-off (tile it-2)
             if (it >= 2) ok = ok && __all_sync(FULL, wait_bar<false>(bar(BAR_SKEMPTY + tb), (use - 1) & 1, abort_flag));
             ok = ok && __all_sync(FULL, wait_bar<true>(bar(BAR_RECV), it & 1, abort_flag));
@@ -417,10 +421,10 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) hp[i] = sigmoid_f(fmaf(gate_par[0], pj[i], gate_par[3 + i]));
                     if (real && hl < C)
-                        ptx::st_async_v4(ptx::mapa(sbase + L.hpre + static_cast<uint32_t>((tb * TILE_M + r) * 16),
+                        ptx::st_async_v4(ptx::mapa(sbase + L.hpre + static_cast<uint32_t>((hs * TILE_M + r) * 16),
                                                    static_cast<uint32_t>(hl)),
                                          hp[0], hp[1], hp[2], hp[3],
-                                         ptx::mapa(bar(BAR_HPRE + tb), static_cast<uint32_t>(hl)));
+                                         ptx::mapa(bar(BAR_HPRE + hs), static_cast<uint32_t>(hl)));
                     if (real && hl < SKF / 4) {
                         // hand-off record: proj[24], inv_rms (picked with constant
                         // indices so that pj stays in registers)
@@ -505,11 +509,10 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
         const int mtid = tid - MIX_WARP0 * 32;          // 0..255
         int it = 0;
         for (int j = cid; j < p.ntiles; j += ncl, ++it) {
-            const int tb = it & 1;
-            const uint32_t use = static_cast<uint32_t>(it >> 1);
             const int64_t t0 = static_cast<int64_t>(j) * TILE_M;
-            const bool ok = __all_sync(FULL, wait_bar<true>(bar(BAR_HPRE + tb), use & 1, abort_flag));
-            const float4* hb = reinterpret_cast<const float4*>(smem + L.hpre) + tb * TILE_M;
+            const int hs = it % NHP;
+            const bool ok = __all_sync(FULL, wait_bar<true>(bar(BAR_HPRE + hs), (it / NHP) & 1, abort_flag));
+            const float4* hb = reinterpret_cast<const float4*>(smem + L.hpre) + hs * TILE_M;
             const int qpt = Dc / 8;
             const int items = ok ? TILE_M * qpt : 0;
             for (int base = 0; base < items; base += NMIX * 32 * 4) {
@@ -545,15 +548,15 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
                     }
                 }
             }
-            // every mix thread is done with this parity's H_pre: arm it for
-            // tile it + 2, then free it at every reducer (which refills it
-            // with st.async)
+            // every mix thread is done with this tile's H_pre buffer: arm it
+            // for tile it + NHP, then free it at every reducer (which refills
+            // it with st.async)
             ptx::fence_proxy_async_smem();
             if (ptx::named_bar_or(3, NMIX * 32, !ok)) break;
             if (warp == MIX_WARP0) {
-                if (lane == 0 && it + 2 < ntl) ptx::mbar_arrive_expect_tx(bar(BAR_HPRE + tb), TILE_M * 16);
+                if (lane == 0 && it + NHP < ntl) ptx::mbar_arrive_expect_tx(bar(BAR_HPRE + hs), TILE_M * 16);
                 __syncwarp();
-                if (lane < C) ptx::mbar_arrive_remote(ptx::mapa(bar(BAR_HFREE + tb), static_cast<uint32_t>(lane)));
+                if (lane < C) ptx::mbar_arrive_remote(ptx::mapa(bar(BAR_HFREE + hs), static_cast<uint32_t>(lane)));
             }
         }
     }
