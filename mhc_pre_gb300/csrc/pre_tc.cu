@@ -90,6 +90,10 @@ constexpr int NTHREADS = 512;                     // 16 warps
 constexpr int GATE_WARP0 = 2, NGATE = 4;          // TMEM readers, cluster reduction, H_pre
 constexpr int SK_WARP = 6;                        // Sinkhorn, other gates, outputs
 constexpr int MIX_WARP0 = 7, NMIX = 9;            // x_in = sum_i H_pre[i] x[i]
+// Token pieces a mix thread loads before it computes (4 streams x 16 B each).
+// Two keep the mix ahead of the tiles; four put so many L2 reads in flight
+// that the TMA stream's boxes land later and the whole kernel slows by 4%.
+constexpr int MIX_UNROLL = 2;
 constexpr int SKF = 28;                           // hand-off record: proj[24], inv_rms (floats)
 constexpr int NHP = 4;                            // H_pre buffers: tiles between reducers and mixes
 constexpr int REC = 25;                           // partial record: 24 logits + sum x^2
@@ -515,12 +519,12 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
             const float4* hb = reinterpret_cast<const float4*>(smem + L.hpre) + hs * TILE_M;
             const int qpt = Dc / 8;
             const int items = ok ? TILE_M * qpt : 0;
-            for (int base = 0; base < items; base += NMIX * 32 * 4) {
-                uint4 xv[4][4];
-                int64_t tok[4];
-                int qq[4], rr[4];
+            for (int base = 0; base < items; base += NMIX * 32 * MIX_UNROLL) {
+                uint4 xv[MIX_UNROLL][4];
+                int64_t tok[MIX_UNROLL];
+                int qq[MIX_UNROLL], rr[MIX_UNROLL];
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
+                for (int m = 0; m < MIX_UNROLL; ++m) {
                     const int idx = base + m * NMIX * 32 + mtid;
                     rr[m] = idx / qpt;
                     qq[m] = idx - rr[m] * qpt;
@@ -532,7 +536,7 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
                     }
                 }
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
+                for (int m = 0; m < MIX_UNROLL; ++m) {
                     if (tok[m] < p.T) {
                         const float4 h = hb[rr[m]];
                         float f0[8], f1[8], f2[8], f3[8], o[8];
