@@ -108,6 +108,31 @@ mhc_status mhc_post(mhc_dtype dt, const void* x, const void* y,
                     int64_t D, void* x_next, cudaStream_t stream);
 
 /*
+ * mhc_post_pre -- mhc_post of layer l followed by mhc_pre of layer l + 1 on
+ * the x_next it stores, in one pass over x and y where the shape allows (the
+ * cross-layer fusion of the inference critical path, section 11.3 of the
+ * openPangu 2.0 notes; each step as in section 5.3):
+ *   x_next = mhc_post(x, y, H_post_l, H_res_l)                (stored in dt)
+ *   (x_in, H_pre, H_post, H_res, proj, inv_rms) = mhc_pre(x_next, phi, b, alpha)
+ *
+ *   x [T, n, D] dt; y [T, D] dt; H_post_l [T, n], H_res_l [T, n, n] float
+ *     (layer l's gates); phi, b, alpha, iters, eps: layer l + 1, as mhc_pre
+ * outputs (written; none may alias an input):
+ *   x_next [T, n, D] dt   bit-identical to mhc_post's
+ *   x_in, H_pre, H_post, H_res, proj, inv_rms   as mhc_pre on the stored x_next
+ * bf16 shapes the fused kernel covers (mhc_kernel_launches("mhc_post_pre",
+ * ...) == 1) take one kernel; every other shape runs mhc_post, then mhc_pre.
+ * Errors as mhc_pre.
+ */
+mhc_status mhc_post_pre(mhc_dtype dt, const void* x, const void* y,
+                        const float* H_post_l, const float* H_res_l,
+                        const float* phi, const float* b, const float* alpha,
+                        int64_t T, int n, int64_t D, int iters, float eps,
+                        void* x_next, void* x_in, float* H_pre, float* H_post,
+                        float* H_res, float* proj, float* inv_rms,
+                        cudaStream_t stream);
+
+/*
  * mhc_post_bwd -- gradients of <g_next, x_next> for mhc_post:
  *   dx[t, j]      = sum_i H_res[t, i, j] g_next[t, i]     (written, not added)
  *   dy[t]         = sum_i H_post[t, i] g_next[t, i]
@@ -123,7 +148,7 @@ mhc_status mhc_post_bwd(mhc_dtype dt, const void* g_next, const void* x,
                         float* dH_post, float* dH_res, cudaStream_t stream);
 
 /* Number of kernels the entry point `op` ("mhc_pre", "mhc_post",
- * "mhc_post_bwd" or "mhc_pre_bwd") launches for these sizes; -1 for an
+ * "mhc_post_pre", "mhc_post_bwd" or "mhc_pre_bwd") launches for these sizes; -1 for an
  * unknown op or sizes the entry point would reject.  Useful when sizing CUDA
  * graphs or counting launches. */
 int mhc_kernel_launches(const char* op, mhc_dtype dt, int64_t T, int n, int64_t D);

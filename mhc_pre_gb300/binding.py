@@ -25,10 +25,11 @@ MHC_F32, MHC_BF16 = 0, 1
 MAX_ITERS = 64
 
 EXPORTS = ("mhc_status_string", "mhc_version", "mhc_get_last_device_error",
-           "mhc_pre", "mhc_post", "mhc_post_bwd", "mhc_kernel_launches",
+           "mhc_pre", "mhc_post", "mhc_post_pre", "mhc_post_bwd", "mhc_kernel_launches",
            "mhc_pre_bwd_workspace_bytes", "mhc_pre_bwd", "mhc_pre_bwd_noalloc")
 
 PreOut = namedtuple("PreOut", "x_in H_pre H_post H_res proj inv_rms")
+PostPreOut = namedtuple("PostPreOut", "x_next x_in H_pre H_post H_res proj inv_rms")
 PostBwdOut = namedtuple("PostBwdOut", "dx dy dH_post dH_res")
 PreBwdOut = namedtuple("PreBwdOut", "dx dphi db dalpha")
 
@@ -40,6 +41,8 @@ _SIGS = {
     "mhc_pre": ([_I, _P, _P, _P, _P, _I64, _I, _I64, _I, _F,
                  _P, _P, _P, _P, _P, _P, _P], _I),
     "mhc_post": ([_I, _P, _P, _P, _P, _I64, _I, _I64, _P, _P], _I),
+    "mhc_post_pre": ([_I, _P, _P, _P, _P, _P, _P, _P, _I64, _I, _I64, _I, _F,
+                      _P, _P, _P, _P, _P, _P, _P, _P], _I),
     "mhc_post_bwd": ([_I, _P, _P, _P, _P, _P, _I64, _I, _I64,
                       _P, _P, _P, _P, _P], _I),
     "mhc_kernel_launches": ([ctypes.c_char_p, _I, _I64, _I, _I64], _I),
@@ -132,6 +135,26 @@ def mhc_pre(x, phi, b, alpha, iters: int = 20, eps: float = 1e-6):
                        _ptr(_f32(b, "b")), _ptr(_f32(alpha, "alpha")), T, n, D,
                        iters, eps, *[_ptr(o) for o in out], _stream(x.device))
     _check(st, "mhc_pre")
+    return out
+
+
+def mhc_post_pre(x, y, H_post_l, H_res_l, phi, b, alpha, iters: int = 20,
+                 eps: float = 1e-6):
+    """mhc_post of layer l, then mhc_pre of layer l + 1 on the stored x_next."""
+    T, n, D = x.shape
+    G = 2 * n + n * n
+    if y.dtype != x.dtype:
+        raise TypeError("x and y must share a dtype")
+    f32 = dict(dtype=torch.float32, device=x.device)
+    out = PostPreOut(torch.empty_like(x), torch.empty((T, D), dtype=x.dtype, device=x.device),
+                     torch.empty((T, n), **f32), torch.empty((T, n), **f32),
+                     torch.empty((T, n, n), **f32), torch.empty((T, G), **f32),
+                     torch.empty((T,), **f32))
+    st = lib().mhc_post_pre(_dtype_code(x), _ptr(x), _ptr(y), _ptr(_f32(H_post_l, "H_post_l")),
+                            _ptr(_f32(H_res_l, "H_res_l")), _ptr(_f32(phi, "phi")),
+                            _ptr(_f32(b, "b")), _ptr(_f32(alpha, "alpha")), T, n, D, iters, eps,
+                            *[_ptr(o) for o in out], _stream(x.device))
+    _check(st, "mhc_post_pre")
     return out
 
 

@@ -53,6 +53,13 @@ cudaError_t launch_pre_tc(const void* x, const float* phi, const float* b, const
                           cudaStream_t s);
 bool pre_tc_supports(int64_t T, int64_t D);
 cudaError_t read_and_clear_device_error(unsigned* word, cudaStream_t s);
+// Defined in post_pre_tc.cu: layer l's residual update fused with layer
+// l + 1's pre forward (bf16).
+bool post_pre_tc_supports(int64_t T, int64_t D);
+cudaError_t launch_post_pre_tc(const void* x, const void* y, const float* H_post_l, const float* H_res_l,
+                               const float* phi, const float* b, const float* alpha, int64_t T, int64_t D,
+                               int iters, float eps, void* x_next, void* x_in, float* H_pre, float* H_post,
+                               float* H_res, float* proj, float* inv_rms, cudaStream_t s);
 }  // namespace mhc
 
 extern "C" {
@@ -113,6 +120,28 @@ mhc_status mhc_post_bwd(mhc_dtype dt, const void* g_next, const void* x, const v
                                           dH_post, dH_res, stream));
 }
 
+mhc_status mhc_post_pre(mhc_dtype dt, const void* x, const void* y, const float* H_post_l,
+                        const float* H_res_l, const float* phi, const float* b, const float* alpha,
+                        int64_t T, int n, int64_t D, int iters, float eps, void* x_next, void* x_in,
+                        float* H_pre, float* H_post, float* H_res, float* proj, float* inv_rms,
+                        cudaStream_t stream) {
+    const void* ptrs[] = {x, y, H_post_l, H_res_l, phi, b, alpha, x_next, x_in,
+                          H_pre, H_post, H_res, proj, inv_rms};
+    mhc_status st = check_common(dt, T, n, D, ptrs, 14);
+    if (st != MHC_OK) return st;
+    if ((st = check_iters(iters)) != MHC_OK) return st;
+    if (!(eps >= 0.0f) || !isfinite(eps)) return MHC_ERR_INVALID_ARG;
+    if (T == 0) return MHC_OK;
+    if (dt == MHC_BF16 && mhc::post_pre_tc_supports(T, D))
+        return from_cuda(mhc::launch_post_pre_tc(x, y, H_post_l, H_res_l, phi, b, alpha, T, D, iters, eps,
+                                                 x_next, x_in, H_pre, H_post, H_res, proj, inv_rms, stream));
+    // other shapes: the two steps one after the other, on the stored x_next
+    st = from_cuda(mhc::launch_post(dt == MHC_BF16, x, y, H_post_l, H_res_l, T, D, x_next, stream));
+    if (st != MHC_OK) return st;
+    return mhc_pre(dt, x_next, phi, b, alpha, T, n, D, iters, eps, x_in, H_pre, H_post, H_res, proj,
+                   inv_rms, stream);
+}
+
 int mhc_kernel_launches(const char* op, mhc_dtype dt, int64_t T, int n, int64_t D) {
     if (op == nullptr) return -1;
     const void* none[] = {nullptr};
@@ -120,6 +149,10 @@ int mhc_kernel_launches(const char* op, mhc_dtype dt, int64_t T, int n, int64_t 
     if (T == 0) return 0;
     if (strcmp(op, "mhc_pre") == 0) return dt == MHC_BF16 && mhc::pre_tc_supports(T, D) ? 1 : 2;
     if (strcmp(op, "mhc_post") == 0 || strcmp(op, "mhc_post_bwd") == 0) return 1;
+    if (strcmp(op, "mhc_post_pre") == 0) {
+        if (dt == MHC_BF16 && mhc::post_pre_tc_supports(T, D)) return 1;
+        return 1 + (dt == MHC_BF16 && mhc::pre_tc_supports(T, D) ? 1 : 2);
+    }
     if (strcmp(op, "mhc_pre_bwd") == 0) return 5;   // both paths: 5 launches
     return -1;
 }

@@ -57,6 +57,7 @@ __device__ unsigned g_device_error;
 
 cudaError_t read_and_clear_bwd_tc_error(unsigned* word);      // pre_bwd_tc.cu
 cudaError_t read_and_clear_bwd_fused_error(unsigned* word);   // pre_bwd_fused.cu
+cudaError_t read_and_clear_post_pre_error(unsigned* word);    // post_pre_tc.cu
 
 cudaError_t read_and_clear_device_error(unsigned* word, cudaStream_t s) {
     cudaError_t e = cudaStreamSynchronize(s);
@@ -72,6 +73,10 @@ cudaError_t read_and_clear_device_error(unsigned* word, cudaStream_t s) {
     *word |= other;
     other = 0;
     e = read_and_clear_bwd_fused_error(&other);
+    if (e != cudaSuccess) return e;
+    *word |= other;
+    other = 0;
+    e = read_and_clear_post_pre_error(&other);
     *word |= other;
     return e;
 }

@@ -214,6 +214,11 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, int32_t x, int32_
                  "r"(x), "r"(y), "r"(src)
                  : "memory");
 }
+__device__ __forceinline__ void tma_store_3d(const void* tmap, int32_t x, int32_t y, int32_t z, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(tmap),
+                 "r"(x), "r"(y), "r"(z), "r"(src)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N bulk groups still read their shared-memory source.
 template <int N>
@@ -291,6 +296,18 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
     d |= static_cast<uint64_t>(1024 >> 4) << 32;                 // stride byte offset: 1024 B
     d |= static_cast<uint64_t>(1) << 46;                         // descriptor version
     d |= static_cast<uint64_t>(2) << 61;                         // 128-byte swizzle
+    return d;
+}
+
+// K-major operand in the 64-byte swizzle: rows of 64 bytes (32 bf16), 8-row
+// groups 512 bytes apart; 16-byte piece q of row r sits at q ^ ((r >> 1) & 3).
+__device__ __forceinline__ uint64_t sw64_kmajor_desc(uint32_t smem_addr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);   // start address >> 4
+    d |= static_cast<uint64_t>(1) << 16;                         // leading byte offset (unused)
+    d |= static_cast<uint64_t>(512 >> 4) << 32;                  // stride byte offset: 512 B
+    d |= static_cast<uint64_t>(1) << 46;                         // descriptor version
+    d |= static_cast<uint64_t>(4) << 61;                         // 64-byte swizzle
     return d;
 }
 

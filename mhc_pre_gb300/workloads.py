@@ -95,3 +95,16 @@ def make_inputs(w: Workload, device="cpu", seed=None):
         out["g_in"] = draw((w.T, w.D), 1.0).to(act)
         out["g_next"] = draw((w.T, w.n, w.D), 1.0).to(act)
     return out
+
+
+def make_layer_gates(w: Workload, device="cpu", seed=None):
+    """Gates of a previous layer for the cross-layer step: H_post [T, n] and
+    H_res [T, n, n] (float32), uniform on (0, 2) and (0, 1/2).  Plain random
+    numbers (the step only combines them linearly); their own generator,
+    seeded 2000 + workload id, so the other inputs stay as they are.
+    """
+    gen = torch.Generator(device=device)
+    gen.manual_seed(2000 + w.wid if seed is None else seed)
+    H_post = torch.rand((w.T, w.n), generator=gen, device=device, dtype=torch.float32).mul_(2.0)
+    H_res = torch.rand((w.T, w.n, w.n), generator=gen, device=device, dtype=torch.float32).mul_(0.5)
+    return {"H_post_l": H_post, "H_res_l": H_res}

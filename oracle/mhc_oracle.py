@@ -159,6 +159,63 @@ def mhc_post(x, y, H_post, H_res):
             + _f64(H_post)[:, :, None] * _f64(y)[:, None, :])
 
 
+def round_to_storage(v, dtype: str):
+    """The value an activation takes when stored: float32 or bfloat16, each
+    round-to-nearest-even from the exact value (the pages compute in fp32 and
+    store activations in the tensor's type).  bfloat16 keeps 8 significant
+    bits and float32's exponent range; values here are far from its limits.
+    """
+    v = _f64(v)
+    if dtype == "f32":
+        return v.astype(np.float32).astype(_F)
+    if dtype != "bf16":
+        raise ValueError(dtype)
+    m, e = np.frexp(v)                      # v = m 2^e, 1/2 <= |m| < 1
+    return np.ldexp(np.rint(m * 256.0) / 256.0, e)   # rint: ties to even
+
+
+def fp32_fma(a, b, c):
+    """float32 fused multiply-add, round(a*b + c) once, for float32-valued
+    a, b, c.  The product of two float32 values is exact in float64; the sum
+    is rounded to float64, then to float32 (one rounding, except when the
+    float64 sum lands exactly halfway between two float32 values, a case of
+    probability about 2^-29 per operation)."""
+    return (_f64(a) * _f64(b) + _f64(c)).astype(np.float32).astype(_F)
+
+
+def mhc_post_stored(x, y, H_post, H_res, store: str):
+    """x_next as an activation of type ``store`` holds it.  The pages compute
+    in float32 and store activations in their type; whether a value rounds up
+    or down to bfloat16 is decided in that float32 precision.  The float32 sum
+    runs in stream order, one rounding per multiply-add:
+    x_next[i] = H_post[i] y + (H_res[i,3] x[3] + (H_res[i,2] x[2]
+                + (H_res[i,1] x[1] + H_res[i,0] x[0])))."""
+    x = _f64(x)
+    Hr = _f64(H_res).astype(np.float32).astype(_F)
+    Hp = _f64(H_post).astype(np.float32).astype(_F)
+    n = x.shape[1]
+    acc = (Hr[:, :, 0, None] * x[:, None, 0, :]).astype(np.float32).astype(_F)
+    for j in range(1, n):
+        acc = fp32_fma(Hr[:, :, j, None], x[:, None, j, :], acc)
+    acc = fp32_fma(Hp[:, :, None], _f64(y)[:, None, :], acc)
+    return round_to_storage(acc, store)
+
+
+def mhc_post_pre(x, y, H_post_l, H_res_l, phi, b, alpha, iters: int, eps: float,
+                 store: str):
+    """Layer l's residual update, then layer l + 1's pre forward on the
+    stored x_next (the cross-layer fusion of the inference critical path,
+    section 11.3 of the openPangu 2.0 notes; each step as in section 5.3).
+
+    ``store`` is the activation type ("bf16" or "f32") x_next is kept in
+    (``mhc_post_stored``).  Returns mhc_pre's dict plus x_next (as stored).
+    """
+    x_next = mhc_post_stored(x, y, H_post_l, H_res_l, store)
+    out = mhc_pre(x_next, phi, b, alpha, iters, eps)
+    out["x_next"] = x_next
+    return out
+
+
 def mhc_post_bwd(g_next, x, y, H_post, H_res):
     """Gradients of <g_next, mhc_post(x, y, H_post, H_res)>.
 

@@ -88,6 +88,25 @@ def run_oracle(inp_np, iters, eps, backward):
     return out
 
 
+POST_PRE_KEYS = ("x_next", "x_in", "H_pre", "H_post", "H_res", "proj", "inv_rms")
+
+
+def run_gpu_post_pre(inp, gates, iters, eps):
+    """The cross-layer step through the C ABI; float64 numpy arrays."""
+    o = B.mhc_post_pre(inp["x"], inp["y"], gates["H_post_l"], gates["H_res_l"], inp["phi"],
+                       inp["b"], inp["alpha"], iters, eps)
+    torch.cuda.synchronize()
+    assert B.get_last_device_error() == B.MHC_OK
+    return {k: f64(getattr(o, k)) for k in POST_PRE_KEYS}
+
+
+def run_oracle_post_pre(inp_np, gates_np, iters, eps, store):
+    """The float64 oracle's cross-layer step on the same inputs."""
+    p = inp_np
+    return O.mhc_post_pre(p["x"], p["y"], gates_np["H_post_l"], gates_np["H_res_l"], p["phi"],
+                          p["b"], p["alpha"], iters, eps, store)
+
+
 GATES = ("H_pre", "H_post", "H_res")
 
 
