@@ -120,9 +120,13 @@ mhc_status mhc_post(mhc_dtype dt, const void* x, const void* y,
  * outputs (written; none may alias an input):
  *   x_next [T, n, D] dt   bit-identical to mhc_post's
  *   x_in, H_pre, H_post, H_res, proj, inv_rms   as mhc_pre on the stored x_next
- * bf16 shapes the fused kernel covers (mhc_kernel_launches("mhc_post_pre",
- * ...) == 1) take one kernel; every other shape runs mhc_post, then mhc_pre.
- * Errors as mhc_pre.
+ *   workspace  device scratch of at least mhc_post_pre_workspace_bytes() bytes,
+ *              16-byte aligned (NULL when that is 0); ws_bytes its size
+ * bf16 shapes the fused kernel covers take two kernels that run at once: the
+ * fused pass, and the x_in mix on the SMs the fused pass leaves free (it
+ * reads each token tile once the fused pass has counted it done in the
+ * workspace).  Every other shape runs mhc_post, then mhc_pre.  Errors as
+ * mhc_pre; MHC_ERR_INVALID_ARG for a missing or short workspace.
  */
 mhc_status mhc_post_pre(mhc_dtype dt, const void* x, const void* y,
                         const float* H_post_l, const float* H_res_l,
@@ -130,7 +134,10 @@ mhc_status mhc_post_pre(mhc_dtype dt, const void* x, const void* y,
                         int64_t T, int n, int64_t D, int iters, float eps,
                         void* x_next, void* x_in, float* H_pre, float* H_post,
                         float* H_res, float* proj, float* inv_rms,
-                        cudaStream_t stream);
+                        void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* Bytes of scratch mhc_post_pre needs for these sizes (0: none). */
+size_t mhc_post_pre_workspace_bytes(mhc_dtype dt, int64_t T, int n, int64_t D);
 
 /*
  * mhc_post_bwd -- gradients of <g_next, x_next> for mhc_post:

@@ -25,7 +25,8 @@ MHC_F32, MHC_BF16 = 0, 1
 MAX_ITERS = 64
 
 EXPORTS = ("mhc_status_string", "mhc_version", "mhc_get_last_device_error",
-           "mhc_pre", "mhc_post", "mhc_post_pre", "mhc_post_bwd", "mhc_kernel_launches",
+           "mhc_pre", "mhc_post", "mhc_post_pre", "mhc_post_pre_workspace_bytes",
+           "mhc_post_bwd", "mhc_kernel_launches",
            "mhc_pre_bwd_workspace_bytes", "mhc_pre_bwd", "mhc_pre_bwd_noalloc")
 
 PreOut = namedtuple("PreOut", "x_in H_pre H_post H_res proj inv_rms")
@@ -42,7 +43,8 @@ _SIGS = {
                  _P, _P, _P, _P, _P, _P, _P], _I),
     "mhc_post": ([_I, _P, _P, _P, _P, _I64, _I, _I64, _P, _P], _I),
     "mhc_post_pre": ([_I, _P, _P, _P, _P, _P, _P, _P, _I64, _I, _I64, _I, _F,
-                      _P, _P, _P, _P, _P, _P, _P, _P], _I),
+                      _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P], _I),
+    "mhc_post_pre_workspace_bytes": ([_I, _I64, _I, _I64], ctypes.c_size_t),
     "mhc_post_bwd": ([_I, _P, _P, _P, _P, _P, _I64, _I, _I64,
                       _P, _P, _P, _P, _P], _I),
     "mhc_kernel_launches": ([ctypes.c_char_p, _I, _I64, _I, _I64], _I),
@@ -150,10 +152,12 @@ def mhc_post_pre(x, y, H_post_l, H_res_l, phi, b, alpha, iters: int = 20,
                      torch.empty((T, n), **f32), torch.empty((T, n), **f32),
                      torch.empty((T, n, n), **f32), torch.empty((T, G), **f32),
                      torch.empty((T,), **f32))
+    nws = int(lib().mhc_post_pre_workspace_bytes(_dtype_code(x), T, n, D))
+    ws = torch.empty((max(nws, 1),), dtype=torch.uint8, device=x.device)
     st = lib().mhc_post_pre(_dtype_code(x), _ptr(x), _ptr(y), _ptr(_f32(H_post_l, "H_post_l")),
                             _ptr(_f32(H_res_l, "H_res_l")), _ptr(_f32(phi, "phi")),
                             _ptr(_f32(b, "b")), _ptr(_f32(alpha, "alpha")), T, n, D, iters, eps,
-                            *[_ptr(o) for o in out], _stream(x.device))
+                            *[_ptr(o) for o in out], _ptr(ws), nws, _stream(x.device))
     _check(st, "mhc_post_pre")
     return out
 

@@ -56,10 +56,11 @@ cudaError_t read_and_clear_device_error(unsigned* word, cudaStream_t s);
 // Defined in post_pre_tc.cu: layer l's residual update fused with layer
 // l + 1's pre forward (bf16).
 bool post_pre_tc_supports(int64_t T, int64_t D);
+size_t post_pre_tc_workspace_bytes(int64_t T);
 cudaError_t launch_post_pre_tc(const void* x, const void* y, const float* H_post_l, const float* H_res_l,
                                const float* phi, const float* b, const float* alpha, int64_t T, int64_t D,
                                int iters, float eps, void* x_next, void* x_in, float* H_pre, float* H_post,
-                               float* H_res, float* proj, float* inv_rms, cudaStream_t s);
+                               float* H_res, float* proj, float* inv_rms, void* workspace, cudaStream_t s);
 }  // namespace mhc
 
 extern "C" {
@@ -120,11 +121,18 @@ mhc_status mhc_post_bwd(mhc_dtype dt, const void* g_next, const void* x, const v
                                           dH_post, dH_res, stream));
 }
 
+size_t mhc_post_pre_workspace_bytes(mhc_dtype dt, int64_t T, int n, int64_t D) {
+    const void* none[] = {nullptr};
+    if (T <= 0 || check_common(dt, T, n, D, none, 0) != MHC_OK) return 0;
+    if (dt == MHC_BF16 && mhc::post_pre_tc_supports(T, D)) return mhc::post_pre_tc_workspace_bytes(T);
+    return 0;
+}
+
 mhc_status mhc_post_pre(mhc_dtype dt, const void* x, const void* y, const float* H_post_l,
                         const float* H_res_l, const float* phi, const float* b, const float* alpha,
                         int64_t T, int n, int64_t D, int iters, float eps, void* x_next, void* x_in,
                         float* H_pre, float* H_post, float* H_res, float* proj, float* inv_rms,
-                        cudaStream_t stream) {
+                        void* workspace, size_t ws_bytes, cudaStream_t stream) {
     const void* ptrs[] = {x, y, H_post_l, H_res_l, phi, b, alpha, x_next, x_in,
                           H_pre, H_post, H_res, proj, inv_rms};
     mhc_status st = check_common(dt, T, n, D, ptrs, 14);
@@ -132,9 +140,14 @@ mhc_status mhc_post_pre(mhc_dtype dt, const void* x, const void* y, const float*
     if ((st = check_iters(iters)) != MHC_OK) return st;
     if (!(eps >= 0.0f) || !isfinite(eps)) return MHC_ERR_INVALID_ARG;
     if (T == 0) return MHC_OK;
-    if (dt == MHC_BF16 && mhc::post_pre_tc_supports(T, D))
+    const size_t need = mhc_post_pre_workspace_bytes(dt, T, n, D);
+    if (need > 0) {
+        if (workspace == nullptr || ws_bytes < need) return MHC_ERR_INVALID_ARG;
+        if (!aligned16(workspace)) return MHC_ERR_MISALIGNED;
         return from_cuda(mhc::launch_post_pre_tc(x, y, H_post_l, H_res_l, phi, b, alpha, T, D, iters, eps,
-                                                 x_next, x_in, H_pre, H_post, H_res, proj, inv_rms, stream));
+                                                 x_next, x_in, H_pre, H_post, H_res, proj, inv_rms, workspace,
+                                                 stream));
+    }
     // other shapes: the two steps one after the other, on the stored x_next
     st = from_cuda(mhc::launch_post(dt == MHC_BF16, x, y, H_post_l, H_res_l, T, D, x_next, stream));
     if (st != MHC_OK) return st;
@@ -150,7 +163,7 @@ int mhc_kernel_launches(const char* op, mhc_dtype dt, int64_t T, int n, int64_t 
     if (strcmp(op, "mhc_pre") == 0) return dt == MHC_BF16 && mhc::pre_tc_supports(T, D) ? 1 : 2;
     if (strcmp(op, "mhc_post") == 0 || strcmp(op, "mhc_post_bwd") == 0) return 1;
     if (strcmp(op, "mhc_post_pre") == 0) {
-        if (dt == MHC_BF16 && mhc::post_pre_tc_supports(T, D)) return 1;
+        if (dt == MHC_BF16 && mhc::post_pre_tc_supports(T, D)) return 2;
         return 1 + (dt == MHC_BF16 && mhc::pre_tc_supports(T, D) ? 1 : 2);
     }
     if (strcmp(op, "mhc_pre_bwd") == 0) return 5;   // both paths: 5 launches

@@ -24,10 +24,15 @@
 //     and the MMA thread have read it.
 //   * The MMA thread projects the slot's two stream pairs against phi and
 //     forms the Gram products, into the same accumulators as pre_tc.
-//   * The mix warps form x_in = sum_i H_pre'[i] x_next[i] over the columns
-//     their own CTA stored, reading x_next back from L2 once the post leader
-//     has seen those stores complete (a TMA store's writes are visible to
-//     plain loads only then).
+//   * x_in = sum_i H_pre'[i] x_next[i] is a second kernel on the SMs the
+//     clusters leave idle (40 of 152 with clusters of 16), launched behind this
+//     one (programmatic dependent launch) so that both run at once.  Each CTA
+//     of a cluster counts a tile done twice in a per-tile word of the
+//     workspace, with release semantics: once its Sinkhorn warp has written
+//     the tile's H_pre', once its x_next stores have completed (a TMA store's
+//     writes are visible to plain loads only then).  The mix kernel reads a
+//     tile (x_next from L2) once its count is complete; it never holds this
+//     kernel up, so it is correct whenever it gets to run.
 //   * Every wait is bounded (about one second); on expiry the kernel latches
 //     the device error word, lets the other roles drain and returns.
 #include <cuda.h>
@@ -68,30 +73,17 @@ constexpr int X_BYTES = 4 * SUB_BYTES;            // x box of a stage: 16 KB
 constexpr int SLOT_BYTES = X_BYTES + SUB_BYTES;   // [x box | y box]: 20 KB
 constexpr int PHI_CHUNK_BYTES = NB * ROW;         // 3 KB
 constexpr int MAX_NCH = 40;                       // K-slice <= 1280 columns
-constexpr int NTHREADS = 512;                     // 16 warps
-constexpr int GATE_WARP0 = 2, NGATE = 4;          // TMEM readers, cluster reduction, mix weights
+constexpr int GATE_WARP0 = 2, NGATE = 4;          // TMEM readers, cluster reduction
 constexpr int SK_WARP = 6;                        // Sinkhorn, other gates, outputs
 #ifndef PP_NPOST
 #define PP_NPOST 4
 #endif
-#ifndef PP_MIXU
-#define PP_MIXU 2
-#endif
-
 constexpr int POST_WARP0 = 7, NPOST = PP_NPOST;   // x_next in the slot
-constexpr int MIX_WARP0 = POST_WARP0 + NPOST;     // x_in: the remaining warps
-constexpr int NMIX = NTHREADS / 32 - MIX_WARP0;
-constexpr int MIX_UNROLL = PP_MIXU;
 constexpr int POST_TPT = NPOST / 2;               // post threads per token
 constexpr int POST_PPT = 4 / POST_TPT;            // 16-byte pieces per post thread and row
 static_assert(NPOST == 2 || NPOST == 4 || NPOST == 8, "post threads split a token row evenly");
+constexpr int NTHREADS = (POST_WARP0 + NPOST) * 32;
 constexpr int SKF = 28;                           // hand-off record: proj[24], inv_rms (floats)
-#ifndef PP_NHP
-#define PP_NHP 4
-#endif
-constexpr int NHP = PP_NHP;                       // H_pre' buffers
-constexpr int HW = 4;                             // H_pre' record (floats)
-constexpr int NST = 8;                            // x_next-stored barriers (tiles in flight)
 constexpr int REC = 25;                           // partial record: 24 logits + sum x^2
 constexpr int RB = 28;                            // its stride in floats
 constexpr uint32_t REC_TX = REC * 4;
@@ -109,23 +101,19 @@ enum : int {
     BAR_ACC_EMPTY = BAR_ACC_FULL + 2,
     BAR_RECV = BAR_ACC_EMPTY + 2,
     BAR_RFREE = BAR_RECV + 1,
-    BAR_HPRE = BAR_RFREE + 1,       // [NHP] H_pre' of a tile arrived
-    BAR_HFREE = BAR_HPRE + NHP,     // [NHP] every CTA's mix is done with that buffer
-    BAR_STORED = BAR_HFREE + NHP,   // [NST] this CTA's x_next stores of a tile are complete
-    BAR_SKFULL = BAR_STORED + NST,
+    BAR_SKFULL = BAR_RFREE + 1,
     BAR_SKEMPTY = BAR_SKFULL + 2,
     NBARS = BAR_SKEMPTY + 2
 };
 
 struct Layout {
-    uint32_t phi, stages, recv, hw, sk, bars, misc, total;
+    uint32_t phi, stages, recv, sk, bars, misc, total;
     __host__ __device__ static Layout make(int nch, int tpc) {
         Layout L;
         L.phi = 0;
         L.stages = (static_cast<uint32_t>(nch) * PHI_CHUNK_BYTES + 1023u) & ~1023u;
         L.recv = L.stages + STAGES * SLOT_BYTES;      // [C senders][TILE_M / C tokens][2 halves][RB]
-        L.hw = L.recv + 2 * TILE_M * RB * 4;          // [NHP][TILE_M][HW]
-        L.sk = L.hw + NHP * TILE_M * HW * 4;          // [2][tpc][SKF]
+        L.sk = L.recv + 2 * TILE_M * RB * 4;          // [2][tpc][SKF]
         L.bars = L.sk + 2 * tpc * SKF * 4;
         L.misc = L.bars + NBARS * 8;
         L.total = L.misc + 64 + 32 * 4;               // tmem slot, abort flag, alpha, b
@@ -145,14 +133,22 @@ struct Params {
     int D, Dc, nch, iters;
     float eps;
     int ntiles;
-    const __nv_bfloat16* x_next;   // written by this kernel's TMA stores, read back by the mix
-    __nv_bfloat16* x_in;
+    unsigned* tile_done;     // [ntiles] completion counts (zeroed before the launch)
     float* H_pre;
     float* H_post;
     float* H_res;
     float* proj;
     float* inv_rms;
 };
+
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
 
 template <bool CLUSTER>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
@@ -188,6 +184,7 @@ post_pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
     float* gate_par = reinterpret_cast<float*>(smem + L.misc + 64);   // alpha[3], b[24]
     const float* recv = reinterpret_cast<const float*>(smem + L.recv);
 
+    ptx::griddep_launch_dependents();   // the mix kernel may start on the idle SMs
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t c = ptx::cluster_ctarank();
     const int cid = static_cast<int>(ptx::cluster_id_x());
@@ -214,12 +211,6 @@ post_pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
         ptx::mbar_init(bar(BAR_RFREE), C);
         // receive barriers are armed one use ahead, before any peer can send
         if (ntl > 0) ptx::mbar_arrive_expect_tx(bar(BAR_RECV), 2 * TILE_M * REC_TX);
-        for (int i = 0; i < NHP; ++i) {
-            ptx::mbar_init(bar(BAR_HPRE + i), 1);
-            ptx::mbar_init(bar(BAR_HFREE + i), C);
-            if (i < ntl) ptx::mbar_arrive_expect_tx(bar(BAR_HPRE + i), TILE_M * HW * 4);
-        }
-        for (int i = 0; i < NST; ++i) ptx::mbar_init(bar(BAR_STORED + i), 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -335,7 +326,8 @@ post_pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
     } else if (warp < SK_WARP) {
         // ------------------------------------------------- gates ----------
         // As in pre_tc.cu: TMEM -> partial records pushed to each token's
-        // reducer; the reducers sum them and push H_pre' to every CTA.
+        // reducer; the reducers sum them and hand the projection to the
+        // Sinkhorn warp.
         const int row = (warp & 3) * 32 + lane;        // TMEM lane quarter = warp % 4
         const int tok = row & (TILE_M - 1), hs = row / TILE_M;   // hs is the same across a warp
         const int half = lane >> 4, hl = lane & 15;    // two tokens per warp, 16 lanes each
@@ -384,10 +376,6 @@ post_pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
                                      recv_bar);
                 ptx::st_async_b32(rec_dst + 4 * NG, ssv, recv_bar);
             }
-            // H_pre' buffer it % NHP is free at every CTA (mix of tile it - NHP done)
-            const int hb = it % NHP;
-            if (it >= NHP)
-                ok = ok && __all_sync(FULL, wait_bar<true>(bar(BAR_HFREE + hb), ((it / NHP) - 1) & 1, abort_flag));
             // the Sinkhorn warp is done with this parity's hand-off (tile it-2)
             if (it >= 2) ok = ok && __all_sync(FULL, wait_bar<false>(bar(BAR_SKEMPTY + tb), (use - 1) & 1, abort_flag));
             ok = ok && __all_sync(FULL, wait_bar<true>(bar(BAR_RECV), it & 1, abort_flag));
@@ -395,7 +383,6 @@ post_pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
                 for (int tt0 = (warp - GATE_WARP0) * 2; tt0 < TPC; tt0 += NGATE * 2) {
                     const int tt = tt0 + half;
                     const bool real = tt < TPC;
-                    const int r = static_cast<int>(c) * TPC + (real ? tt : 0);
                     float va = 0.f, vb = 0.f;
                     if (real) {
 #pragma unroll
@@ -415,15 +402,6 @@ post_pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
                     const float inv = 1.0f / sqrtf(sq / static_cast<float>(K) + p.eps);
 #pragma unroll
                     for (int g = 0; g < NG; ++g) pj[g] *= inv;
-                    // the pre gates of layer l + 1 (same expression as in token_gates)
-                    float hp[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) hp[i] = sigmoid_f(fmaf(gate_par[0], pj[i], gate_par[3 + i]));
-                    if (real && hl < C)
-                        ptx::st_async_v4(ptx::mapa(sbase + L.hw + static_cast<uint32_t>((hb * TILE_M + r) * HW * 4),
-                                                   static_cast<uint32_t>(hl)),
-                                         hp[0], hp[1], hp[2], hp[3],
-                                         ptx::mapa(bar(BAR_HPRE + hb), static_cast<uint32_t>(hl)));
                     if (real && hl < SKF / 4) {
                         // hand-off record: proj[24], inv_rms
                         float4 o = make_float4(inv, 0.f, 0.f, 0.f);
@@ -494,9 +472,14 @@ post_pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
                 }
             }
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(BAR_SKEMPTY + tb));
+            if (lane == 0) {
+                ptx::mbar_arrive(bar(BAR_SKEMPTY + tb));
+                // this CTA's H_pre' of the tile is written
+                __threadfence();
+                red_release_add(p.tile_done + j, 1u);
+            }
         }
-    } else if (warp < MIX_WARP0) {
+    } else {
         // --------------------------------------------------- post ---------
         // x_next = H_res x + H_post y, in place in the slot: POST_TPT threads
         // per token, each with POST_PPT of the row's four 16-byte pieces (8
@@ -571,10 +554,10 @@ post_pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
                     ptx::mbar_arrive(bar(BAR_EMPTY + stage));
                     if (sub == 0 && it > 0) {
                         // every store of the previous tile has completed: the mix
-                        // may read that x_next back with plain loads
+                        // kernel may read that x_next back with plain loads
                         ptx::bulk_wait<1>();
                         asm volatile("fence.proxy.async.global;" ::: "memory");
-                        ptx::mbar_arrive(bar(BAR_STORED + (it - 1) % NST));
+                        red_release_add(p.tile_done + (j - ncl), 1u);
                     }
                 }
                 if (++stage == STAGES) { stage = 0; ++round; }
@@ -583,71 +566,7 @@ post_pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
         if (leader && it > 0) {
             ptx::bulk_wait<0>();
             asm volatile("fence.proxy.async.global;" ::: "memory");
-            ptx::mbar_arrive(bar(BAR_STORED + (it - 1) % NST));
-        }
-    } else {
-        // --------------------------------------------------- mix ----------
-        // x_in = sum_i H_pre'[i] x_next[i] (mhc_pre's sum) over the columns
-        // this CTA stored: its cpd interleaved 32-column chunks of each stream,
-        // read back from L2.
-        const int mtid = tid - MIX_WARP0 * 32;
-        int it = 0;
-        for (int j = cid; j < p.ntiles; j += ncl, ++it) {
-            const int64_t t0 = static_cast<int64_t>(j) * TILE_M;
-            const int hb = it % NHP;
-            const bool ok = __all_sync(FULL, wait_bar<true>(bar(BAR_HPRE + hb), (it / NHP) & 1, abort_flag) &&
-                                                 wait_bar<false>(bar(BAR_STORED + it % NST), (it / NST) & 1, abort_flag));
-            const float4* hpb = reinterpret_cast<const float4*>(smem + L.hw) + hb * TILE_M;
-            const int ppt = cpd * (KW / 8);                // 16-byte pieces per token and stream
-            const int items = ok ? TILE_M * ppt : 0;
-            for (int base = 0; base < items; base += NMIX * 32 * MIX_UNROLL) {
-                uint4 xv[MIX_UNROLL][4];
-                int64_t tok[MIX_UNROLL];
-                int col[MIX_UNROLL], rr[MIX_UNROLL];
-#pragma unroll
-                for (int m = 0; m < MIX_UNROLL; ++m) {
-                    const int idx = base + m * NMIX * 32 + mtid;
-                    rr[m] = idx / ppt;
-                    const int pc = idx - rr[m] * ppt;         // (chunk, piece)
-                    col[m] = ((pc / (KW / 8)) * C + static_cast<int>(c)) * KW + (pc % (KW / 8)) * 8;
-                    tok[m] = (idx < items) ? t0 + rr[m] : p.T;
-                    if (tok[m] < p.T) {
-                        const __nv_bfloat16* src = p.x_next + tok[m] * K + col[m];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) xv[m][i] = ld16_stream(src + static_cast<int64_t>(i) * D);
-                    }
-                }
-#pragma unroll
-                for (int m = 0; m < MIX_UNROLL; ++m) {
-                    if (tok[m] < p.T) {
-                        const float4 h = hpb[rr[m]];
-                        float f0[8], f1[8], f2[8], f3[8], o[8];
-                        Vec<__nv_bfloat16>::unpack(xv[m][0], f0);
-                        Vec<__nv_bfloat16>::unpack(xv[m][1], f1);
-                        Vec<__nv_bfloat16>::unpack(xv[m][2], f2);
-                        Vec<__nv_bfloat16>::unpack(xv[m][3], f3);
-#pragma unroll
-                        for (int q = 0; q < 8; q += 2) {
-                            float2 a = __fmul2_rn(make_float2(h.x, h.x), make_float2(f0[q], f0[q + 1]));
-                            a = __ffma2_rn(make_float2(h.y, h.y), make_float2(f1[q], f1[q + 1]), a);
-                            a = __ffma2_rn(make_float2(h.z, h.z), make_float2(f2[q], f2[q + 1]), a);
-                            a = __ffma2_rn(make_float2(h.w, h.w), make_float2(f3[q], f3[q + 1]), a);
-                            o[q] = a.x;
-                            o[q + 1] = a.y;
-                        }
-                        st16_stream(p.x_in + tok[m] * D + col[m], Vec<__nv_bfloat16>::pack(o));
-                    }
-                }
-            }
-            // every mix thread is done with this tile's H_pre': arm the buffer
-            // for tile it + NHP, then free it at every reducer
-            ptx::fence_proxy_async_smem();
-            if (ptx::named_bar_or(3, NMIX * 32, !ok)) break;
-            if (warp == MIX_WARP0) {
-                if (lane == 0 && it + NHP < ntl) ptx::mbar_arrive_expect_tx(bar(BAR_HPRE + hb), TILE_M * HW * 4);
-                __syncwarp();
-                if (lane < C) ptx::mbar_arrive_remote(ptx::mapa(bar(BAR_HFREE + hb), static_cast<uint32_t>(lane)));
-            }
+            red_release_add(p.tile_done + (cid + (it - 1) * ncl), 1u);
         }
     }
 done:
@@ -665,6 +584,88 @@ done:
         ptx::tmem_dealloc(tmem_base, TMEM_COLS);
     }
     ptx::cluster_sync();
+}
+
+// ------------------------------------------------------------------ mix ----
+// x_in = sum_i H_pre'[i] x_next[i] (mhc_pre's sum), on the SMs the cluster
+// kernel leaves idle.  Eight CTAs share a tile, MIX_TOK tokens each, and the
+// groups of eight take tiles in turn, so a few tiles are in flight, each read
+// back from L2 soon after the cluster kernel stored it.  One CTA per SM: its
+// dynamic shared memory keeps a second one (and a cluster CTA) off the SM.
+constexpr int MIX_THREADS = 512;
+constexpr int MIX_GROUP = 8;                      // CTAs per tile
+constexpr int MIX_TOK = TILE_M / MIX_GROUP;       // tokens per CTA and tile
+constexpr int MIX_UNROLL = 5;
+constexpr size_t MIX_SMEM = 116 * 1024;
+
+__global__ void __launch_bounds__(MIX_THREADS, 1)
+post_pre_mix_kernel(const __nv_bfloat16* __restrict__ x_next, const float* H_pre, __nv_bfloat16* __restrict__ x_in,
+                    const unsigned* tile_done, unsigned need, int64_t T, int D, int ntiles) {
+    __shared__ float4 hp[MIX_TOK];
+    __shared__ int stop;
+    const int tid = threadIdx.x;
+    const int ngroups = static_cast<int>(gridDim.x) / MIX_GROUP;
+    const int group = static_cast<int>(blockIdx.x) / MIX_GROUP, part = static_cast<int>(blockIdx.x) % MIX_GROUP;
+    const int64_t K = 4ll * D;
+    const int qpt = D / 8;                         // 16-byte pieces per stream row
+    if (tid == 0) stop = 0;
+    __syncthreads();
+    for (int j = group; group < ngroups && j < ntiles; j += ngroups) {
+        const int64_t t0 = static_cast<int64_t>(j) * TILE_M + part * MIX_TOK;
+        const int nt = T - t0 < MIX_TOK ? static_cast<int>(T - t0) : MIX_TOK;
+        if (nt <= 0) continue;
+        if (tid == 0) {
+            // every CTA of the tile's cluster has written its H_pre' and
+            // completed its x_next stores (acquire pairs with their release)
+            const uint64_t w0 = ptx::globaltimer();
+            while (ld_acquire(tile_done + j) < need) {
+                if (ptx::globaltimer() - w0 > WAIT_LIMIT_NS) {
+                    atomicOr(&g_post_pre_error, 2u);
+                    stop = 1;
+                    break;
+                }
+                __nanosleep(128);
+            }
+        }
+        __syncthreads();
+        if (stop) break;
+        if (tid < nt) hp[tid] = __ldcg(reinterpret_cast<const float4*>(H_pre) + t0 + tid);
+        __syncthreads();
+        const int items = nt * qpt;
+        for (int base = 0; base < items; base += MIX_THREADS * MIX_UNROLL) {
+            uint4 xv[MIX_UNROLL][4];
+            int rr[MIX_UNROLL], qq[MIX_UNROLL];
+#pragma unroll
+            for (int m = 0; m < MIX_UNROLL; ++m) {
+                const int idx = base + m * MIX_THREADS + tid;
+                rr[m] = idx < items ? idx / qpt : -1;
+                qq[m] = idx - (idx / qpt) * qpt;
+                if (rr[m] >= 0) {
+                    const uint4* src = reinterpret_cast<const uint4*>(x_next + (t0 + rr[m]) * K + qq[m] * 8);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) xv[m][i] = __ldcg(src + static_cast<int64_t>(i) * (D / 8));
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < MIX_UNROLL; ++m) {
+                if (rr[m] >= 0) {
+                    const float4 h = hp[rr[m]];
+                    float f0[8], f1[8], f2[8], f3[8], o[8];
+                    Vec<__nv_bfloat16>::unpack(xv[m][0], f0);
+                    Vec<__nv_bfloat16>::unpack(xv[m][1], f1);
+                    Vec<__nv_bfloat16>::unpack(xv[m][2], f2);
+                    Vec<__nv_bfloat16>::unpack(xv[m][3], f3);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        o[q] = fmaf(h.w, f3[q], fmaf(h.z, f2[q], fmaf(h.y, f1[q], h.x * f0[q])));
+                    st16_stream(x_in + (t0 + rr[m]) * D + qq[m] * 8, Vec<__nv_bfloat16>::pack(o));
+                }
+            }
+        }
+        __syncthreads();   // hp is refilled for the next tile
+    }
+    // complete only after the cluster kernel (its other outputs) has
+    if (tid == 0) ptx::griddep_wait();
 }
 
 // ------------------------------------------------------------------ host ---
@@ -769,6 +770,11 @@ bool encode_y(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* tm, const v
 
 }  // namespace pp
 
+size_t post_pre_tc_workspace_bytes(int64_t T) {
+    const int64_t ntiles = (T + pp::TILE_M - 1) / pp::TILE_M;
+    return static_cast<size_t>((ntiles * 4 + 255) / 256 * 256);
+}
+
 bool post_pre_tc_supports(int64_t T, int64_t D) {
     if (T < pp::TILE_M || D > (int64_t(1) << 20) || T >= (int64_t(1) << 31)) return false;
     if (4 * D * T >= (int64_t(1) << 46)) return false;
@@ -779,7 +785,7 @@ bool post_pre_tc_supports(int64_t T, int64_t D) {
 cudaError_t launch_post_pre_tc(const void* x, const void* y, const float* H_post_l, const float* H_res_l,
                                const float* phi, const float* b, const float* alpha, int64_t T, int64_t D,
                                int iters, float eps, void* x_next, void* x_in, float* H_pre, float* H_post,
-                               float* H_res, float* proj, float* inv_rms, cudaStream_t s) {
+                               float* H_res, float* proj, float* inv_rms, void* workspace, cudaStream_t s) {
     const int C = pp::cluster_for(D);
     auto encode = tensor_map_encoder();
     if (C == 0 || encode == nullptr) return cudaErrorNotSupported;
@@ -802,8 +808,7 @@ cudaError_t launch_post_pre_tc(const void* x, const void* y, const float* H_post
     prm.iters = iters;
     prm.eps = eps;
     prm.ntiles = static_cast<int>((T + pp::TILE_M - 1) / pp::TILE_M);
-    prm.x_next = static_cast<const __nv_bfloat16*>(x_next);
-    prm.x_in = static_cast<__nv_bfloat16*>(x_in);
+    prm.tile_done = static_cast<unsigned*>(workspace);
     prm.H_pre = H_pre;
     prm.H_post = H_post;
     prm.H_res = H_res;
@@ -813,13 +818,47 @@ cudaError_t launch_post_pre_tc(const void* x, const void* y, const float* H_post
     int ncl = pp::max_clusters_for(C);
     if (ncl <= 0) return cudaErrorNotSupported;
     if (ncl > prm.ntiles) ncl = prm.ntiles;
+    cudaError_t e = cudaMemsetAsync(workspace, 0, static_cast<size_t>(prm.ntiles) * 4, s);
+    if (e != cudaSuccess) return e;
     switch (C) {
-        case 16: return pp::launch<16>(tx, ty, txn, prm, ncl, smem, s);
-        case 8: return pp::launch<8>(tx, ty, txn, prm, ncl, smem, s);
-        case 4: return pp::launch<4>(tx, ty, txn, prm, ncl, smem, s);
-        case 2: return pp::launch<2>(tx, ty, txn, prm, ncl, smem, s);
+        case 16: e = pp::launch<16>(tx, ty, txn, prm, ncl, smem, s); break;
+        case 8: e = pp::launch<8>(tx, ty, txn, prm, ncl, smem, s); break;
+        case 4: e = pp::launch<4>(tx, ty, txn, prm, ncl, smem, s); break;
+        case 2: e = pp::launch<2>(tx, ty, txn, prm, ncl, smem, s); break;
+        default: e = cudaErrorNotSupported;
     }
-    return cudaErrorNotSupported;
+    if (e != cudaSuccess) return e;
+    // the mix kernel: on the SMs the clusters leave free, in groups of eight
+    // CTAs (all SMs when none is free: it then runs after the cluster kernel)
+    int dev = 0, nsm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(pp::post_pre_mix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(pp::MIX_SMEM));
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    int free_sm = nsm - ncl * C;
+    if (free_sm < pp::MIX_GROUP) free_sm = nsm;
+    int ngroups = free_sm / pp::MIX_GROUP;
+    if (ngroups > prm.ntiles) ngroups = prm.ntiles;
+    if (ngroups < 1) ngroups = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ngroups * pp::MIX_GROUP));
+    cfg.blockDim = dim3(pp::MIX_THREADS);
+    cfg.dynamicSmemBytes = pp::MIX_SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, pp::post_pre_mix_kernel, static_cast<const __nv_bfloat16*>(x_next),
+                              static_cast<const float*>(H_pre), static_cast<__nv_bfloat16*>(x_in),
+                              static_cast<const unsigned*>(workspace), static_cast<unsigned>(2 * C), T,
+                              static_cast<int>(D), prm.ntiles);
 }
 
 }  // namespace mhc
