@@ -46,6 +46,8 @@ def parse_args():
     p.add_argument("--tokens", type=int, default=None,
                    help="override the workload's T (smaller cases for profiling)")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cross-layer", action="store_true",
+                   help="skip the side measurement of mhc_post_pre")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     return p.parse_args()
 
@@ -80,6 +82,53 @@ def algorithmic_bytes(w):
     per_launch = {"mhc_pre": 4 * K * G, "mhc_post": 0, "mhc_post_bwd": 0,
                   "mhc_pre_bwd": 2 * 4 * K * G}
     return {op: per_tok[op] * T + per_launch[op] for op in STEP_OPS}, per_tok
+
+
+def cross_layer_bytes(w):
+    """Bytes mhc_post_pre must move per launch: x, y and layer l's gates in,
+    x_next, x_in, layer l + 1's gates and saved state out, phi once."""
+    a = 2 if w.dtype == "bf16" else 4
+    per_tok = (a * w.K + a * w.D + 4 * (w.n + w.n * w.n) + a * w.K + a * w.D
+               + 4 * (w.n + w.n + w.n * w.n + w.G + 1))
+    return per_tok * w.T + 4 * w.K * w.G, per_tok
+
+
+def run_cross_layer(w, inp, dev, reps=20):
+    """mhc_post_pre (layer l's residual update fused with layer l + 1's pre
+    step) against mhc_post then mhc_pre, CUDA events on the stream, inputs
+    larger than L2.  A side measurement: not part of the timed step."""
+    import torch
+    from mhc_pre_gb300 import binding as B
+    from mhc_pre_gb300 import workloads as W
+    g = W.make_layer_gates(w, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fused():
+        B.mhc_post_pre(inp["x"], inp["y"], g["H_post_l"], g["H_res_l"], inp["phi"], inp["b"],
+                       inp["alpha"], w.iters, w.eps)
+
+    def separate():
+        xn = B.mhc_post(inp["x"], inp["y"], g["H_post_l"], g["H_res_l"])
+        B.mhc_pre(xn, inp["phi"], inp["b"], inp["alpha"], w.iters, w.eps)
+
+    out = {}
+    for name, f in (("fused", fused), ("separate", separate)):
+        for _ in range(3):
+            f()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(reps):
+            f()
+        e.record(stream)
+        torch.cuda.synchronize()
+        out[name] = s.elapsed_time(e) / reps
+    assert B.get_last_device_error() == B.MHC_OK
+    nb, per_tok = cross_layer_bytes(w)
+    peak, kind = peaks()
+    return {"op": "mhc_post_pre", "fused_ms": out["fused"], "separate_ms": out["separate"],
+            "GBps": nb / out["fused"] / 1e6, "frac_of_" + kind: nb / out["fused"] / 1e6 / peak,
+            "algorithmic_bytes_per_token": per_tok,
+            "launches": B.kernel_launches("mhc_post_pre", w.dtype, w.T, w.n, w.D)}
 
 
 class ClockSampler:
@@ -292,6 +341,11 @@ def main():
     if not args.no_e2e:
         e2e = run_e2e(args, w, inp, step, stream, dev, world)
 
+    # ---- side measurement: the cross-layer step (rank 0, N = 1) --------------
+    cross = None
+    if rank == 0 and world == 1 and not args.no_cross_layer:
+        cross = run_cross_layer(w, inp, dev)
+
     # ---- float64 oracle on the host cores (rank 0, N = 1) --------------------
     cpu = None
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
@@ -321,6 +375,7 @@ def main():
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
+        "cross_layer": cross,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
