@@ -776,7 +776,7 @@ size_t post_pre_tc_workspace_bytes(int64_t T) {
 }
 
 bool post_pre_tc_supports(int64_t T, int64_t D) {
-    if (T < pp::TILE_M || D > (int64_t(1) << 20) || T >= (int64_t(1) << 31)) return false;
+    if (T < 1 || D > (int64_t(1) << 20) || T >= (int64_t(1) << 31)) return false;
     if (4 * D * T >= (int64_t(1) << 46)) return false;
     const int C = pp::cluster_for(D);
     return C != 0 && tensor_map_encoder() != nullptr && pp::max_clusters_for(C) > 0;

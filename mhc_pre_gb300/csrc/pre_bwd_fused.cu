@@ -709,7 +709,7 @@ bool encode_2d(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* tm, const 
 }  // namespace bwdfu
 
 bool pre_bwd_fused_supports(int64_t T, int64_t D) {
-    if (T < bwdfu::TT || T >= (int64_t(1) << 31) || 4 * D * T >= (int64_t(1) << 46)) return false;
+    if (T < 1 || T >= (int64_t(1) << 31) || 4 * D * T >= (int64_t(1) << 46)) return false;
     const int C = bwdfu::cluster_for(D);
     return C > 0 && tensor_map_encoder() != nullptr && bwdfu::max_clusters(C) > 0;
 }

@@ -679,7 +679,8 @@ cudaError_t launch(const CUtensorMap& tm, const Params& prm, int nclusters, size
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() { return tc::encode_fn(); }
 
 bool pre_tc_supports(int64_t T, int64_t D) {
-    if (T < tc::TILE_M || D > (int64_t(1) << 20)) return false;
+    // T < 64 is one partial tile: TMA fills the rows past T with zeros
+    if (T < 1 || D > (int64_t(1) << 20)) return false;
     if (4 * D * T >= (int64_t(1) << 46)) return false;
     const int C = tc::cluster_for(D);
     if (C == 0 || tc::encode_fn() == nullptr) return false;

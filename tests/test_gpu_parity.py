@@ -66,6 +66,8 @@ def test_workload4_bf16_fwd_bwd_s4096():
     # and one (6144) that the one-pass backward does not take
     (64, 256, "bf16"), (150, 320, "bf16"), (100, 3072, "bf16"), (160, 6144, "bf16"),
     (1, 4, "f32"), (67, 12, "f32"), (130, 260, "f32"),
+    # fewer tokens than one 64-token tile (decode-sized batches)
+    (2, 5120, "bf16"), (17, 5120, "bf16"), (63, 2560, "bf16"), (5, 1024, "bf16"),
 ])
 def test_ragged_shapes_fwd_bwd(T, D, dtype):
     w = W.WORKLOADS[4].with_(T=T, D=D, dtype=dtype, wid=40 + T % 50)

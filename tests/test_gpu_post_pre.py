@@ -44,8 +44,10 @@ def test_post_pre_workloads(wid):
 
 @pytest.mark.parametrize("T,D,dtype", [
     (129, 5120, "bf16"), (333, 2560, "bf16"), (200, 1024, "bf16"), (64, 256, "bf16"),
+    # fewer tokens than one tile
+    (1, 5120, "bf16"), (17, 5120, "bf16"), (63, 2560, "bf16"),
     # shapes the fused kernel does not take: mhc_post, then mhc_pre
-    (1, 5120, "bf16"), (65, 40, "bf16"), (67, 12, "f32"),
+    (65, 40, "bf16"), (67, 12, "f32"),
 ])
 def test_post_pre_ragged_and_fallback_shapes(T, D, dtype):
     _check(W.WORKLOADS[4].with_(T=T, D=D, dtype=dtype, wid=60 + T % 30))
