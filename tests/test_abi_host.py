@@ -79,6 +79,31 @@ def test_pre_validation(L):
                      None, None, None, None, None, None, None) == B.MHC_OK
 
 
+def _post_pre(L, dt=B.MHC_BF16, x=A, T=8, n=4, D=64, iters=20, eps=1e-6, outs=None, ws=A, nws=4096):
+    outs = outs or [A] * 7
+    return L.mhc_post_pre(dt, x, A, A, A, A, A, A, T, n, D, iters, eps, *outs, ws, nws, None)
+
+
+def test_post_pre_validation(L):
+    assert _post_pre(L, n=3) == B.MHC_ERR_UNSUPPORTED
+    assert _post_pre(L, D=60) == B.MHC_ERR_UNSUPPORTED
+    assert _post_pre(L, dt=7) == B.MHC_ERR_INVALID_ARG
+    assert _post_pre(L, T=-1) == B.MHC_ERR_INVALID_ARG
+    assert _post_pre(L, x=None) == B.MHC_ERR_INVALID_ARG
+    assert _post_pre(L, x=MIS) == B.MHC_ERR_MISALIGNED
+    assert _post_pre(L, outs=[A, A, A, A, MIS, A, A]) == B.MHC_ERR_MISALIGNED
+    assert _post_pre(L, iters=0) == B.MHC_ERR_INVALID_ARG
+    assert _post_pre(L, iters=B.MAX_ITERS + 1) == B.MHC_ERR_UNSUPPORTED
+    assert _post_pre(L, eps=float("nan")) == B.MHC_ERR_INVALID_ARG
+    # T = 0 is a no-op that touches nothing, even with null pointers
+    assert L.mhc_post_pre(B.MHC_BF16, *([None] * 7), 0, 4, 64, 20, 1e-6, *([None] * 7),
+                          None, 0, None) == B.MHC_OK
+    # shapes the fused kernel never takes need no workspace
+    assert L.mhc_post_pre_workspace_bytes(B.MHC_F32, 64, 4, 256) == 0
+    assert L.mhc_post_pre_workspace_bytes(B.MHC_BF16, 0, 4, 5120) == 0
+    assert L.mhc_post_pre_workspace_bytes(B.MHC_BF16, 64, 4, 60) == 0
+
+
 def test_post_and_post_bwd_validation(L):
     assert L.mhc_post(B.MHC_BF16, A, A, A, A, 4, 2, 64, A, None) == B.MHC_ERR_UNSUPPORTED
     assert L.mhc_post(B.MHC_BF16, A, None, A, A, 4, 4, 64, A, None) == B.MHC_ERR_INVALID_ARG
