@@ -231,6 +231,54 @@ def mhc_post_bwd(g_next, x, y, H_post, H_res):
     return dict(dx=dx, dy=dy, dH_post=dH_post, dH_res=dH_res)
 
 
+SANDWICH_NORM, BLOCK_NORM = 1, 2
+
+
+def mhc_post_norm(x, y, H_post, H_res, flags: int, eps: float):
+    """The residual update with openPangu's stability changes (section 5.4 of
+    the openPangu 2.0 notes), each optional (bit of ``flags``):
+      SANDWICH_NORM: the sublayer output y is RMS-normalised over D before
+        the H_post write-back;
+      BLOCK_NORM: the updated multi-stream state is RMS-normalised over its
+        flattened n*D row (the extent of the layer's own RMSNorm).
+    Unit weights, eps inside the square root.  Returns dict x_next
+    [T, n, D], inv_rms_y [T], inv_rms_out [T] (1 where a step is off).
+    """
+    x, y = _f64(x), _f64(y)
+    T = x.shape[0]
+    if flags & SANDWICH_NORM:
+        inv_rms_y = 1.0 / np.sqrt(np.mean(y * y, axis=1) + eps)
+    else:
+        inv_rms_y = np.ones(T)
+    z = mhc_post(x, y * inv_rms_y[:, None], H_post, H_res)
+    if flags & BLOCK_NORM:
+        x_next, inv_rms_out = rmsnorm_flat(z, eps)
+    else:
+        x_next, inv_rms_out = z, np.ones(T)
+    return dict(x_next=x_next, inv_rms_y=inv_rms_y, inv_rms_out=inv_rms_out)
+
+
+def _rmsnorm_vjp(g, u, inv_rms, axes):
+    """Reverse mode of u = z * inv_rms(z) (RMSNorm with unit weight over
+    ``axes``): dz = inv_rms (g - u <g, u> / N), N the normalised extent."""
+    N = int(np.prod([g.shape[a] for a in axes]))
+    c = np.sum(g * u, axis=axes, keepdims=True)
+    shape = [g.shape[0]] + [1] * (g.ndim - 1)
+    return inv_rms.reshape(shape) * (g - u * c / N)
+
+
+def mhc_post_norm_bwd(g_next, x, y, H_post, H_res, flags: int, eps: float):
+    """Gradients of <g_next, x_next> for mhc_post_norm, by the chain rule
+    through its steps.  Returns dict dx, dy, dH_post, dH_res."""
+    f = mhc_post_norm(x, y, H_post, H_res, flags, eps)
+    g = _f64(g_next)
+    dz = _rmsnorm_vjp(g, f["x_next"], f["inv_rms_out"], (1, 2)) if flags & BLOCK_NORM else g
+    yn = _f64(y) * f["inv_rms_y"][:, None]
+    pb = mhc_post_bwd(dz, x, yn, H_post, H_res)
+    dy = _rmsnorm_vjp(pb["dy"], yn, f["inv_rms_y"], (1,)) if flags & SANDWICH_NORM else pb["dy"]
+    return dict(dx=pb["dx"], dy=dy, dH_post=pb["dH_post"], dH_res=pb["dH_res"])
+
+
 def mhc_pre_bwd(g_in, dH_post, dH_res, x, phi, b, alpha, iters: int,
                 eps: float):
     """Gradients of <g_in, x_in> + (terms reaching H_post, H_res).
