@@ -108,6 +108,44 @@ mhc_status mhc_post(mhc_dtype dt, const void* x, const void* y,
                     int64_t D, void* x_next, cudaStream_t stream);
 
 /*
+ * mhc_post_norm -- the residual update with openPangu's stability changes
+ * (section 5.4 of the openPangu 2.0 notes), each selected by a bit of `flags`:
+ *   MHC_POST_SANDWICH_NORM  y' = y r_y, r_y = 1/sqrt(mean_D(y^2) + eps): the
+ *                           sublayer output normalised before the H_post
+ *                           write-back ("sandwich normalisation");
+ *   MHC_POST_BLOCK_NORM     x_next = z s, z = H_res x + H_post y',
+ *                           s = 1/sqrt(mean_{n*D}(z^2) + eps): the updated
+ *                           multi-stream state normalised ("block-level
+ *                           post-normalisation"; the pages apply it after
+ *                           the first layer and every fifth one).
+ * Unit weights; eps inside the square root.  flags = 0 is mhc_post.
+ *
+ *   x [T, n, D] dt; y [T, D] dt; H_post [T, n], H_res [T, n, n] float
+ * outputs (written): x_next [T, n, D] dt; inv_rms_y [T], inv_rms_out [T]
+ *   float (r_y and s, 1 where the step is off; saved for the backward).
+ * MHC_ERR_INVALID_ARG for flags outside 0..3; MHC_ERR_UNSUPPORTED when D is
+ * above 8192 (bf16) or 4096 (float32).
+ */
+#define MHC_POST_SANDWICH_NORM 1
+#define MHC_POST_BLOCK_NORM 2
+mhc_status mhc_post_norm(mhc_dtype dt, const void* x, const void* y,
+                         const float* H_post, const float* H_res, int flags,
+                         float eps, int64_t T, int n, int64_t D, void* x_next,
+                         float* inv_rms_y, float* inv_rms_out, cudaStream_t stream);
+
+/*
+ * mhc_post_norm_bwd -- gradients of <g_next, x_next> for mhc_post_norm with
+ * the same flags, eps and the saved inv_rms_y, inv_rms_out:
+ *   dx, dy written (not added); dH_post [T, n], dH_res [T, n, n] written.
+ */
+mhc_status mhc_post_norm_bwd(mhc_dtype dt, const void* g_next, const void* x,
+                             const void* y, const float* H_post,
+                             const float* H_res, int flags, float eps,
+                             const float* inv_rms_y, const float* inv_rms_out,
+                             int64_t T, int n, int64_t D, void* dx, void* dy,
+                             float* dH_post, float* dH_res, cudaStream_t stream);
+
+/*
  * mhc_post_pre -- mhc_post of layer l followed by mhc_pre of layer l + 1 on
  * the x_next it stores, in one pass over x and y where the shape allows (the
  * cross-layer fusion of the inference critical path, section 11.3 of the
@@ -155,7 +193,8 @@ mhc_status mhc_post_bwd(mhc_dtype dt, const void* g_next, const void* x,
                         float* dH_post, float* dH_res, cudaStream_t stream);
 
 /* Number of kernels the entry point `op` ("mhc_pre", "mhc_post",
- * "mhc_post_pre", "mhc_post_bwd" or "mhc_pre_bwd") launches for these sizes; -1 for an
+ * "mhc_post_norm", "mhc_post_norm_bwd", "mhc_post_pre", "mhc_post_bwd" or
+ * "mhc_pre_bwd") launches for these sizes; -1 for an
  * unknown op or sizes the entry point would reject.  Useful when sizing CUDA
  * graphs or counting launches. */
 int mhc_kernel_launches(const char* op, mhc_dtype dt, int64_t T, int n, int64_t D);

@@ -25,12 +25,15 @@ MHC_F32, MHC_BF16 = 0, 1
 MAX_ITERS = 64
 
 EXPORTS = ("mhc_status_string", "mhc_version", "mhc_get_last_device_error",
-           "mhc_pre", "mhc_post", "mhc_post_pre", "mhc_post_pre_workspace_bytes",
+           "mhc_pre", "mhc_post", "mhc_post_norm", "mhc_post_norm_bwd",
+           "mhc_post_pre", "mhc_post_pre_workspace_bytes",
            "mhc_post_bwd", "mhc_kernel_launches",
            "mhc_pre_bwd_workspace_bytes", "mhc_pre_bwd", "mhc_pre_bwd_noalloc")
 
 PreOut = namedtuple("PreOut", "x_in H_pre H_post H_res proj inv_rms")
 PostPreOut = namedtuple("PostPreOut", "x_next x_in H_pre H_post H_res proj inv_rms")
+PostNormOut = namedtuple("PostNormOut", "x_next inv_rms_y inv_rms_out")
+SANDWICH_NORM, BLOCK_NORM = 1, 2
 PostBwdOut = namedtuple("PostBwdOut", "dx dy dH_post dH_res")
 PreBwdOut = namedtuple("PreBwdOut", "dx dphi db dalpha")
 
@@ -45,6 +48,9 @@ _SIGS = {
     "mhc_post_pre": ([_I, _P, _P, _P, _P, _P, _P, _P, _I64, _I, _I64, _I, _F,
                       _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P], _I),
     "mhc_post_pre_workspace_bytes": ([_I, _I64, _I, _I64], ctypes.c_size_t),
+    "mhc_post_norm": ([_I, _P, _P, _P, _P, _I, _F, _I64, _I, _I64, _P, _P, _P, _P], _I),
+    "mhc_post_norm_bwd": ([_I, _P, _P, _P, _P, _P, _I, _F, _P, _P, _I64, _I, _I64,
+                           _P, _P, _P, _P, _P], _I),
     "mhc_post_bwd": ([_I, _P, _P, _P, _P, _P, _I64, _I, _I64,
                       _P, _P, _P, _P, _P], _I),
     "mhc_kernel_launches": ([ctypes.c_char_p, _I, _I64, _I, _I64], _I),
@@ -159,6 +165,35 @@ def mhc_post_pre(x, y, H_post_l, H_res_l, phi, b, alpha, iters: int = 20,
                             _ptr(_f32(b, "b")), _ptr(_f32(alpha, "alpha")), T, n, D, iters, eps,
                             *[_ptr(o) for o in out], _ptr(ws), nws, _stream(x.device))
     _check(st, "mhc_post_pre")
+    return out
+
+
+def mhc_post_norm(x, y, H_post, H_res, flags: int, eps: float = 1e-6):
+    """mhc_post with the sandwich (flag 1) and block (flag 2) normalisations."""
+    T, n, D = x.shape
+    if y.dtype != x.dtype:
+        raise TypeError("x and y must share a dtype")
+    f32 = dict(dtype=torch.float32, device=x.device)
+    out = PostNormOut(torch.empty_like(x), torch.empty((T,), **f32), torch.empty((T,), **f32))
+    st = lib().mhc_post_norm(_dtype_code(x), _ptr(x), _ptr(y), _ptr(_f32(H_post, "H_post")),
+                             _ptr(_f32(H_res, "H_res")), flags, eps, T, n, D, *[_ptr(o) for o in out],
+                             _stream(x.device))
+    _check(st, "mhc_post_norm")
+    return out
+
+
+def mhc_post_norm_bwd(g_next, x, y, H_post, H_res, flags: int, inv_rms_y, inv_rms_out,
+                      eps: float = 1e-6):
+    """Gradients of <g_next, x_next> for mhc_post_norm: (dx, dy, dH_post, dH_res)."""
+    T, n, D = x.shape
+    f32 = dict(dtype=torch.float32, device=x.device)
+    out = PostBwdOut(torch.empty_like(x), torch.empty_like(y), torch.empty((T, n), **f32),
+                     torch.empty((T, n, n), **f32))
+    st = lib().mhc_post_norm_bwd(_dtype_code(x), _ptr(g_next), _ptr(x), _ptr(y),
+                                 _ptr(_f32(H_post, "H_post")), _ptr(_f32(H_res, "H_res")), flags, eps,
+                                 _ptr(_f32(inv_rms_y, "inv_rms_y")), _ptr(_f32(inv_rms_out, "inv_rms_out")),
+                                 T, n, D, *[_ptr(o) for o in out], _stream(x.device))
+    _check(st, "mhc_post_norm_bwd")
     return out
 
 

@@ -40,6 +40,16 @@ cudaError_t launch_post(bool bf16, const void* x, const void* y, const float* H_
                         const float* H_res, int64_t T, int64_t D, void* x_next,
                         cudaStream_t s);
 
+// The residual update with openPangu's stability changes (post_norm.cu).
+bool post_norm_supports(bool bf16, int64_t D);
+cudaError_t launch_post_norm(bool bf16, const void* x, const void* y, const float* H_post, const float* H_res,
+                             int flags, float eps, int64_t T, int64_t D, void* x_next, float* inv_rms_y,
+                             float* inv_rms_out, cudaStream_t s);
+cudaError_t launch_post_norm_bwd(bool bf16, const void* g_next, const void* x, const void* y, const float* H_post,
+                                 const float* H_res, int flags, float eps, const float* inv_rms_y,
+                                 const float* inv_rms_out, int64_t T, int64_t D, void* dx, void* dy,
+                                 float* dH_post, float* dH_res, cudaStream_t s);
+
 cudaError_t launch_post_bwd(bool bf16, const void* g, const void* x, const void* y,
                             const float* H_post, const float* H_res, int64_t T, int64_t D,
                             void* dx, void* dy, float* dH_post, float* dH_res,

@@ -111,6 +111,36 @@ mhc_status mhc_post(mhc_dtype dt, const void* x, const void* y, const float* H_p
     return from_cuda(mhc::launch_post(dt == MHC_BF16, x, y, H_post, H_res, T, D, x_next, stream));
 }
 
+mhc_status mhc_post_norm(mhc_dtype dt, const void* x, const void* y, const float* H_post,
+                         const float* H_res, int flags, float eps, int64_t T, int n, int64_t D,
+                         void* x_next, float* inv_rms_y, float* inv_rms_out, cudaStream_t stream) {
+    const void* ptrs[] = {x, y, H_post, H_res, x_next, inv_rms_y, inv_rms_out};
+    mhc_status st = check_common(dt, T, n, D, ptrs, 7);
+    if (st != MHC_OK) return st;
+    if (flags < 0 || flags > (MHC_POST_SANDWICH_NORM | MHC_POST_BLOCK_NORM)) return MHC_ERR_INVALID_ARG;
+    if (!(eps >= 0.0f) || !isfinite(eps)) return MHC_ERR_INVALID_ARG;
+    if (!mhc::post_norm_supports(dt == MHC_BF16, D)) return MHC_ERR_UNSUPPORTED;
+    if (T == 0) return MHC_OK;
+    return from_cuda(mhc::launch_post_norm(dt == MHC_BF16, x, y, H_post, H_res, flags, eps, T, D, x_next,
+                                           inv_rms_y, inv_rms_out, stream));
+}
+
+mhc_status mhc_post_norm_bwd(mhc_dtype dt, const void* g_next, const void* x, const void* y,
+                             const float* H_post, const float* H_res, int flags, float eps,
+                             const float* inv_rms_y, const float* inv_rms_out, int64_t T, int n,
+                             int64_t D, void* dx, void* dy, float* dH_post, float* dH_res,
+                             cudaStream_t stream) {
+    const void* ptrs[] = {g_next, x, y, H_post, H_res, inv_rms_y, inv_rms_out, dx, dy, dH_post, dH_res};
+    mhc_status st = check_common(dt, T, n, D, ptrs, 11);
+    if (st != MHC_OK) return st;
+    if (flags < 0 || flags > (MHC_POST_SANDWICH_NORM | MHC_POST_BLOCK_NORM)) return MHC_ERR_INVALID_ARG;
+    if (!(eps >= 0.0f) || !isfinite(eps)) return MHC_ERR_INVALID_ARG;
+    if (!mhc::post_norm_supports(dt == MHC_BF16, D)) return MHC_ERR_UNSUPPORTED;
+    if (T == 0) return MHC_OK;
+    return from_cuda(mhc::launch_post_norm_bwd(dt == MHC_BF16, g_next, x, y, H_post, H_res, flags, eps, inv_rms_y,
+                                               inv_rms_out, T, D, dx, dy, dH_post, dH_res, stream));
+}
+
 mhc_status mhc_post_bwd(mhc_dtype dt, const void* g_next, const void* x, const void* y,
                         const float* H_post, const float* H_res, int64_t T, int n, int64_t D,
                         void* dx, void* dy, float* dH_post, float* dH_res, cudaStream_t stream) {
@@ -162,6 +192,8 @@ int mhc_kernel_launches(const char* op, mhc_dtype dt, int64_t T, int n, int64_t 
     if (T == 0) return 0;
     if (strcmp(op, "mhc_pre") == 0) return dt == MHC_BF16 && mhc::pre_tc_supports(T, D) ? 1 : 2;
     if (strcmp(op, "mhc_post") == 0 || strcmp(op, "mhc_post_bwd") == 0) return 1;
+    if (strcmp(op, "mhc_post_norm") == 0 || strcmp(op, "mhc_post_norm_bwd") == 0)
+        return mhc::post_norm_supports(dt == MHC_BF16, D) ? 1 : -1;
     if (strcmp(op, "mhc_post_pre") == 0) {
         if (dt == MHC_BF16 && mhc::post_pre_tc_supports(T, D)) return 2;
         return 1 + (dt == MHC_BF16 && mhc::pre_tc_supports(T, D) ? 1 : 2);

@@ -26,16 +26,16 @@
 //     tens of cycles at best.  Accumulators live in TMEM, two of each, so
 //     the next tile's MMAs overlap this tile's epilogue.
 //   * Four gate warps read each token's two partial records (one per
-//     stream of a pair) from TMEM and push them, with the partial sum of squares, into the shared memory of the
-//     CTA that reduces that token (st.async completing on the receiver's
-//     mbarrier: no fences).  Each CTA reduces 64/C tokens over the C
+//     stream of a pair) from TMEM and push them, with the partial sum of
+//     squares, into the shared memory of the CTA that reduces that token
+//     (st.async completing on the receiver's mbarrier: no fences).  Each CTA reduces 64/C tokens over the C
 //     partials, computes H_pre first and pushes it to every CTA of the
 //     cluster the same way, and only then runs the other gates and Sinkhorn
 //     and writes them out.  Credit barriers (records read, H_pre used) let
 //     consecutive tiles overlap without a cluster-wide rendezvous.
-//   * Eight mix warps form x_in = sum_i H_pre[i] x[i] over the CTA's D-slice:
-//     x is read from HBM once (TMA, kept in L2 with an evict-last hint) and a
-//     second time, soon after, for the mix.
+//   * Nine mix warps form x_in = sum_i H_pre[i] x[i] over the CTA's D-slice:
+//     x is read from HBM once (TMA, normal L2 priority) and a second time,
+//     soon after, for the mix, from L2.
 //   * Every wait is bounded (about one second); on expiry the kernel latches
 //     the device error word, lets the other roles drain and returns.
 #include <cuda.h>
