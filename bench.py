@@ -47,7 +47,7 @@ def parse_args():
                    help="override the workload's T (smaller cases for profiling)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cross-layer", action="store_true",
-                   help="skip the side measurement of mhc_post_pre")
+                   help="skip the side measurements (mhc_post_pre, mhc_post_norm)")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     return p.parse_args()
 
@@ -129,6 +129,44 @@ def run_cross_layer(w, inp, dev, reps=20):
             "GBps": nb / out["fused"] / 1e6, "frac_of_" + kind: nb / out["fused"] / 1e6 / peak,
             "algorithmic_bytes_per_token": per_tok,
             "launches": B.kernel_launches("mhc_post_pre", w.dtype, w.T, w.n, w.D)}
+
+
+def run_post_norm(w, inp, dev, reps=10):
+    """mhc_post_norm / mhc_post_norm_bwd with both stability steps (sandwich
+    and block normalisation) on the step's inputs: a side measurement, not
+    part of the timed step.  Bytes: x, y, gates in and x_next out (forward);
+    g_next, x, y, gates in and dx, dy, dH out (backward); saved r_y, s."""
+    import torch
+    from mhc_pre_gb300 import binding as B
+    from mhc_pre_gb300 import workloads as W
+    g = W.make_layer_gates(w, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flags = B.SANDWICH_NORM | B.BLOCK_NORM
+    f = B.mhc_post_norm(inp["x"], inp["y"], g["H_post_l"], g["H_res_l"], flags, w.eps)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(reps):
+            fn()
+        e.record(stream)
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) / reps
+
+    fwd = timed(lambda: B.mhc_post_norm(inp["x"], inp["y"], g["H_post_l"], g["H_res_l"], flags, w.eps))
+    bwd = timed(lambda: B.mhc_post_norm_bwd(inp["g_next"], inp["x"], inp["y"], g["H_post_l"], g["H_res_l"],
+                                            flags, f.inv_rms_y, f.inv_rms_out, w.eps))
+    assert B.get_last_device_error() == B.MHC_OK
+    a = 2 if w.dtype == "bf16" else 4
+    gates = 4 * (w.n + w.n * w.n)
+    fb = w.T * (2 * a * w.K + a * w.D + gates + 8)
+    bb = w.T * (3 * a * w.K + 2 * a * w.D + 2 * gates + 8)
+    peak, kind = peaks()
+    return {"op": "mhc_post_norm (sandwich + block)", "fwd_ms": fwd, "bwd_ms": bwd,
+            "fwd_GBps": fb / fwd / 1e6, "bwd_GBps": bb / bwd / 1e6,
+            "fwd_frac_of_" + kind: fb / fwd / 1e6 / peak, "bwd_frac_of_" + kind: bb / bwd / 1e6 / peak}
 
 
 class ClockSampler:
@@ -342,9 +380,10 @@ def main():
         e2e = run_e2e(args, w, inp, step, stream, dev, world)
 
     # ---- side measurement: the cross-layer step (rank 0, N = 1) --------------
-    cross = None
+    cross = post_norm = None
     if rank == 0 and world == 1 and not args.no_cross_layer:
         cross = run_cross_layer(w, inp, dev)
+        post_norm = run_post_norm(w, inp, dev)
 
     # ---- float64 oracle on the host cores (rank 0, N = 1) --------------------
     cpu = None
@@ -376,6 +415,7 @@ def main():
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "cross_layer": cross,
+        "post_norm": post_norm,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
