@@ -425,7 +425,7 @@ def main():
 
 
 def launches(w):
-    """Kernels of this library launched per step (kernels)."""
+    """Kernels of this library launched per step (mhc_kernel_launches of each op)."""
     from mhc_pre_gb300 import binding as B
     return sum(B.kernel_launches(op, w.dtype, w.T, w.n, w.D) for op in STEP_OPS)
 

@@ -13,7 +13,7 @@ The Ascend mHC Triton operator article adds that H_res is doubly stochastic
 (non-negative, every row and column summing to 1) and that H_pre / H_post read
 n streams into one and write one stream back to n.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
   * W_mHC is called ``phi`` here, stored [K, G] with K index k = i*D + d
     (stream-major flattening of h_bar).
   * Each logit group has one scalar scale alpha and every logit a bias b:

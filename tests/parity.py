@@ -1,6 +1,6 @@
 """Helpers for GPU-vs-oracle parity tests (test infrastructure).
 
-Tolerances (the layer's stated bar; derivation in the design doc):
+Tolerances (the layer's stated bar):
   * float32 activations: max |gpu - ref| <= 1e-5 on every output (scaled by
     the output's largest magnitude for the reductions dH_post, dH_res, dphi,
     db, dalpha);
