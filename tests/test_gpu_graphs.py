@@ -1,0 +1,75 @@
+"""The library's calls inside CUDA graphs: a whole fwd+bwd step, and the
+cross-layer step (a memset, a cluster kernel and a second kernel launched
+with programmatic dependent launch), captured once and replayed, give the
+same bits as the same calls run eagerly."""
+
+import pytest
+import torch
+
+from mhc_pre_gb300 import binding as B
+from mhc_pre_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda", 0)
+
+
+def _step(a, w, ws):
+    f = B.mhc_pre(a["x"], a["phi"], a["b"], a["alpha"], w.iters, w.eps)
+    xn = B.mhc_post(a["x"], a["y"], f.H_post, f.H_res)
+    pb = B.mhc_post_bwd(a["g_next"], a["x"], a["y"], f.H_post, f.H_res)
+    qb = B.mhc_pre_bwd(a["g_in"], pb.dH_post, pb.dH_res, a["x"], a["phi"], a["b"], a["alpha"],
+                       f.proj, f.inv_rms, pb.dx, w.iters, workspace=ws)
+    return [f.x_in, f.H_pre, f.H_res, xn, pb.dy, qb.dx, qb.dphi, qb.db, qb.dalpha]
+
+
+def test_step_in_a_cuda_graph_matches_eager():
+    dev = _dev()
+    w = W.WORKLOADS[4].with_(T=1000)
+    a = W.make_inputs(w, device=dev)
+    ws = torch.empty((B.pre_bwd_workspace_bytes(torch.bfloat16, w.T, w.n, w.D),), dtype=torch.uint8, device=dev)
+    eager = [t.clone() for t in _step(a, w, ws)]
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        _step(a, w, ws)              # warm-up on the capture stream
+    torch.cuda.current_stream(dev).wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        out = _step(a, w, ws)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert B.get_last_device_error() == B.MHC_OK
+    for e, o in zip(eager, out):
+        assert torch.equal(e, o)
+
+
+def test_cross_layer_step_in_a_cuda_graph_matches_eager():
+    dev = _dev()
+    w = W.WORKLOADS[2].with_(T=2000)
+    a = W.make_inputs(w, device=dev)
+    gates = W.make_layer_gates(w, device=dev)
+    run = lambda: B.mhc_post_pre(a["x"], a["y"], gates["H_post_l"], gates["H_res_l"], a["phi"], a["b"],
+                                 a["alpha"], w.iters, w.eps)
+    eager = [t.clone() for t in run()]
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        run()
+    torch.cuda.current_stream(dev).wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        out = run()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert B.get_last_device_error() == B.MHC_OK
+    for e, o in zip(eager, out):
+        assert torch.equal(e, o)
