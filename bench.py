@@ -266,7 +266,8 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(w, S),
+        "config": workload_config(w),      # the same workload as the CUDA arm ...
+        "sample_tokens_per_step": S,        # ... of which each step times a bounded sample
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"float64 NumPy oracle, fwd+bwd of the whole layer on {S} "
                                    f"tokens per step of the {w.name} workload"},
