@@ -47,7 +47,8 @@ def parse_args():
                    help="override the workload's T (smaller cases for profiling)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cross-layer", action="store_true",
-                   help="skip the side measurements (mhc_post_pre, mhc_post_norm)")
+                   help="skip the side measurements (mhc_post_pre, mhc_post_norm, "
+                        "the recompute backward)")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     return p.parse_args()
 
@@ -167,6 +168,52 @@ def run_post_norm(w, inp, dev, reps=10):
     return {"op": "mhc_post_norm (sandwich + block)", "fwd_ms": fwd, "bwd_ms": bwd,
             "fwd_GBps": fb / fwd / 1e6, "bwd_GBps": bb / bwd / 1e6,
             "fwd_frac_of_" + kind: fb / fwd / 1e6 / peak, "bwd_frac_of_" + kind: bb / bwd / 1e6 / peak}
+
+
+def run_recompute(w, inp, dev, reps=10):
+    """The recompute-oriented backward on the step's inputs: mhc_pre_gates
+    (the gates and saved state from x alone) and mhc_layer_bwd_recompute
+    against mhc_post_bwd + mhc_pre_bwd on saved state.  A side measurement,
+    not part of the timed step."""
+    import torch
+    from mhc_pre_gb300 import binding as B
+    stream = torch.cuda.current_stream(dev)
+    x, y, phi, b, alpha = (inp[k] for k in ("x", "y", "phi", "b", "alpha"))
+    f = B.mhc_pre(x, phi, b, alpha, w.iters, w.eps)
+    ws = torch.empty((B.layer_bwd_recompute_workspace_bytes(x.dtype, w.T, w.n, w.D),),
+                     dtype=torch.uint8, device=dev)
+    ws_bwd = torch.empty((B.pre_bwd_workspace_bytes(x.dtype, w.T, w.n, w.D),), dtype=torch.uint8, device=dev)
+
+    def saved():
+        pb = B.mhc_post_bwd(inp["g_next"], x, y, f.H_post, f.H_res)
+        B.mhc_pre_bwd(inp["g_in"], pb.dH_post, pb.dH_res, x, phi, b, alpha, f.proj, f.inv_rms, pb.dx,
+                      w.iters, workspace=ws_bwd)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(reps):
+            fn()
+        e.record(stream)
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) / reps
+
+    gates = timed(lambda: B.mhc_pre_gates(x, phi, b, alpha, w.iters, w.eps))
+    rec = timed(lambda: B.mhc_layer_bwd_recompute(inp["g_in"], inp["g_next"], x, y, phi, b, alpha,
+                                                  w.iters, w.eps, workspace=ws))
+    sav = timed(saved)
+    assert B.get_last_device_error() == B.MHC_OK
+    a = 2 if w.dtype == "bf16" else 4
+    saved_state = 4 * (w.G + 1)                                   # proj, inv_rms
+    gb = w.T * (a * w.K + 4 * (w.n + w.n + w.n * w.n) + saved_state) + 4 * w.K * w.G
+    peak, kind = peaks()
+    return {"op": "mhc_pre_gates, mhc_layer_bwd_recompute", "gates_ms": gates,
+            "gates_GBps": gb / gates / 1e6, "gates_frac_of_" + kind: gb / gates / 1e6 / peak,
+            "bwd_recompute_ms": rec, "bwd_saved_state_ms": sav,
+            "saved_state_bytes_per_token": {"saved": saved_state, "recompute": 0},
+            "launches": B.kernel_launches("mhc_layer_bwd_recompute", w.dtype, w.T, w.n, w.D)}
 
 
 class ClockSampler:
@@ -381,10 +428,11 @@ def main():
         e2e = run_e2e(args, w, inp, step, stream, dev, world)
 
     # ---- side measurement: the cross-layer step (rank 0, N = 1) --------------
-    cross = post_norm = None
+    cross = post_norm = recompute = None
     if rank == 0 and world == 1 and not args.no_cross_layer:
         cross = run_cross_layer(w, inp, dev)
         post_norm = run_post_norm(w, inp, dev)
+        recompute = run_recompute(w, inp, dev)
 
     # ---- float64 oracle on the host cores (rank 0, N = 1) --------------------
     cpu = None
@@ -417,6 +465,7 @@ def main():
         "clocks": clocks,
         "cross_layer": cross,
         "post_norm": post_norm,
+        "recompute": recompute,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -192,9 +192,9 @@ mhc_status mhc_post_bwd(mhc_dtype dt, const void* g_next, const void* x,
                         int64_t T, int n, int64_t D, void* dx, void* dy,
                         float* dH_post, float* dH_res, cudaStream_t stream);
 
-/* Number of kernels the entry point `op` ("mhc_pre", "mhc_post",
- * "mhc_post_norm", "mhc_post_norm_bwd", "mhc_post_pre", "mhc_post_bwd" or
- * "mhc_pre_bwd") launches for these sizes; -1 for an
+/* Number of kernels the entry point `op` ("mhc_pre", "mhc_pre_gates",
+ * "mhc_post", "mhc_post_norm", "mhc_post_norm_bwd", "mhc_post_pre",
+ * "mhc_post_bwd", "mhc_pre_bwd" or "mhc_layer_bwd_recompute") launches for these sizes; -1 for an
  * unknown op or sizes the entry point would reject.  Useful when sizing CUDA
  * graphs or counting launches. */
 int mhc_kernel_launches(const char* op, mhc_dtype dt, int64_t T, int n, int64_t D);
@@ -272,6 +272,69 @@ mhc_status mhc_pre_bwd_noalloc(mhc_dtype dt, const void* g_in, const float* dH_p
                                const float* inv_rms, int64_t T, int n, int64_t D, int iters,
                                void* dx, float* dphi, float* db, float* dalpha,
                                cudaStream_t stream);
+
+/*
+ * Recompute-oriented backward.  The Ascend mHC Triton operator article
+ * (paragraphs on the activation memory of mHC and on recompute inside a
+ * layer and across layers) keeps, for each mHC layer, only the input of
+ * hc_pre (the multi-stream state x) and the sublayer's output y, and
+ * recomputes everything else during the backward.  The two calls below do
+ * that: mhc_pre_gates recomputes the gates and the saved state from x, and
+ * mhc_layer_bwd_recompute is the whole layer's backward from (x, y) and the
+ * incoming gradients.  Across layers, x of layer l + 1 is restored from
+ * layer l's (x, y) with mhc_post_pre (or mhc_pre_gates, then mhc_post).
+ */
+
+/*
+ * mhc_pre_gates -- mhc_pre without the H_pre mix: the same kernel and the
+ * same arithmetic, so H_pre, H_post, H_res, proj and inv_rms are bit for bit
+ * those mhc_pre writes for the same inputs.  x_in is neither computed nor
+ * written.  Arguments, layouts, ownership and errors as mhc_pre.
+ */
+mhc_status mhc_pre_gates(mhc_dtype dt, const void* x, const float* phi,
+                         const float* b, const float* alpha, int64_t T, int n,
+                         int64_t D, int iters, float eps, float* H_pre,
+                         float* H_post, float* H_res, float* proj,
+                         float* inv_rms, cudaStream_t stream);
+
+/* Bytes of scratch mhc_layer_bwd_recompute needs (0 for T = 0): the
+ * recomputed gates and saved state (196 B per token), dH_post and dH_res
+ * (80 B per token), each region rounded up to 256 B, then
+ * mhc_pre_bwd_workspace_bytes(). */
+size_t mhc_layer_bwd_recompute_workspace_bytes(mhc_dtype dt, int64_t T, int n,
+                                               int64_t D);
+
+/*
+ * mhc_layer_bwd_recompute -- the backward of one mHC layer (mhc_pre, the
+ * sublayer's output y, mhc_post) from its inputs alone:
+ *   mhc_pre_gates(x)   -> H_pre, H_post, H_res, proj, inv_rms   (scratch)
+ *   mhc_post_bwd       -> dx (written), dy, dH_post, dH_res     (dH: scratch)
+ *   mhc_pre_bwd        -> dx (accumulated), dphi, db, dalpha
+ * on `stream`, in that order.  The results are bit for bit those of
+ * mhc_post_bwd then mhc_pre_bwd given the state a mhc_pre call on the same x
+ * saved.
+ *
+ *   g_in    [T, D]     dt      dL/dx_in
+ *   g_next  [T, n, D]  dt      dL/dx_next
+ *   x, phi, b, alpha, iters, eps   as passed to mhc_pre
+ *   y       [T, D]     dt      the sublayer output, as passed to mhc_post
+ * outputs (written):
+ *   dx      [T, n, D]  dt      dL/dx (both paths)
+ *   dy      [T, D]     dt      dL/dy
+ *   dphi    [n*D, G]   float
+ *   db      [G]        float
+ *   dalpha  [3]        float
+ *   workspace, ws_bytes        device scratch of at least
+ *                              mhc_layer_bwd_recompute_workspace_bytes() bytes
+ * Errors as mhc_pre_bwd; MHC_ERR_INVALID_ARG for a missing or short
+ * workspace.  Data parallelism as mhc_pre_bwd.
+ */
+mhc_status mhc_layer_bwd_recompute(mhc_dtype dt, const void* g_in, const void* g_next,
+                                   const void* x, const void* y, const float* phi,
+                                   const float* b, const float* alpha, int64_t T, int n,
+                                   int64_t D, int iters, float eps, void* dx, void* dy,
+                                   float* dphi, float* db, float* dalpha, void* workspace,
+                                   size_t ws_bytes, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -28,7 +28,9 @@ EXPORTS = ("mhc_status_string", "mhc_version", "mhc_get_last_device_error",
            "mhc_pre", "mhc_post", "mhc_post_norm", "mhc_post_norm_bwd",
            "mhc_post_pre", "mhc_post_pre_workspace_bytes",
            "mhc_post_bwd", "mhc_kernel_launches",
-           "mhc_pre_bwd_workspace_bytes", "mhc_pre_bwd", "mhc_pre_bwd_noalloc")
+           "mhc_pre_bwd_workspace_bytes", "mhc_pre_bwd", "mhc_pre_bwd_noalloc",
+           "mhc_pre_gates", "mhc_layer_bwd_recompute_workspace_bytes",
+           "mhc_layer_bwd_recompute")
 
 PreOut = namedtuple("PreOut", "x_in H_pre H_post H_res proj inv_rms")
 PostPreOut = namedtuple("PostPreOut", "x_next x_in H_pre H_post H_res proj inv_rms")
@@ -36,6 +38,8 @@ PostNormOut = namedtuple("PostNormOut", "x_next inv_rms_y inv_rms_out")
 SANDWICH_NORM, BLOCK_NORM = 1, 2
 PostBwdOut = namedtuple("PostBwdOut", "dx dy dH_post dH_res")
 PreBwdOut = namedtuple("PreBwdOut", "dx dphi db dalpha")
+PreGatesOut = namedtuple("PreGatesOut", "H_pre H_post H_res proj inv_rms")
+LayerBwdOut = namedtuple("LayerBwdOut", "dx dy dphi db dalpha")
 
 _P, _I64, _I, _F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
 _SIGS = {
@@ -59,6 +63,11 @@ _SIGS = {
                      _I, _P, _P, _P, _P, _P, ctypes.c_size_t, _P], _I),
     "mhc_pre_bwd_noalloc": ([_I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I,
                              _I64, _I, _P, _P, _P, _P, _P], _I),
+    "mhc_pre_gates": ([_I, _P, _P, _P, _P, _I64, _I, _I64, _I, _F,
+                       _P, _P, _P, _P, _P, _P], _I),
+    "mhc_layer_bwd_recompute_workspace_bytes": ([_I, _I64, _I, _I64], ctypes.c_size_t),
+    "mhc_layer_bwd_recompute": ([_I, _P, _P, _P, _P, _P, _P, _P, _I64, _I, _I64, _I, _F,
+                                 _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P], _I),
 }
 
 _lib = None
@@ -144,6 +153,56 @@ def mhc_pre(x, phi, b, alpha, iters: int = 20, eps: float = 1e-6):
                        iters, eps, *[_ptr(o) for o in out], _stream(x.device))
     _check(st, "mhc_pre")
     return out
+
+
+def mhc_pre_gates(x, phi, b, alpha, iters: int = 20, eps: float = 1e-6):
+    """mhc_pre without the H_pre mix (no x_in): the gates and the saved state,
+    bit for bit as mhc_pre writes them."""
+    T, n, D = x.shape
+    G = 2 * n + n * n
+    f32 = dict(dtype=torch.float32, device=x.device)
+    out = PreGatesOut(torch.empty((T, n), **f32), torch.empty((T, n), **f32),
+                      torch.empty((T, n, n), **f32), torch.empty((T, G), **f32),
+                      torch.empty((T,), **f32))
+    st = lib().mhc_pre_gates(_dtype_code(x), _ptr(x), _ptr(_f32(phi, "phi")),
+                             _ptr(_f32(b, "b")), _ptr(_f32(alpha, "alpha")), T, n, D,
+                             iters, eps, *[_ptr(o) for o in out], _stream(x.device))
+    _check(st, "mhc_pre_gates")
+    return out
+
+
+def layer_bwd_recompute_workspace_bytes(dtype, T: int, n: int, D: int) -> int:
+    code = MHC_BF16 if dtype == torch.bfloat16 else MHC_F32
+    return int(lib().mhc_layer_bwd_recompute_workspace_bytes(code, T, n, D))
+
+
+def mhc_layer_bwd_recompute(g_in, g_next, x, y, phi, b, alpha, iters: int = 20,
+                            eps: float = 1e-6, workspace=None):
+    """The layer's backward from its inputs x and y alone (the gates and the
+    saved state recomputed).  Returns dx, dy, dphi, db, dalpha."""
+    T, n, D = x.shape
+    G = 2 * n + n * n
+    if not (g_in.dtype == g_next.dtype == x.dtype == y.dtype):
+        raise TypeError("g_in, g_next, x and y must share a dtype")
+    need = layer_bwd_recompute_workspace_bytes(x.dtype, T, n, D)
+    if workspace is None:
+        workspace = torch.empty((max(need, 16),), dtype=torch.uint8, device=x.device)
+    f32 = dict(dtype=torch.float32, device=x.device)
+    dx = torch.empty_like(x)
+    dy = torch.empty_like(y)
+    dphi = torch.empty((n * D, G), **f32)
+    db = torch.empty((G,), **f32)
+    dalpha = torch.empty((3,), **f32)
+    st = lib().mhc_layer_bwd_recompute(
+        _dtype_code(x), _ptr(g_in), _ptr(g_next), _ptr(x), _ptr(y), _ptr(_f32(phi, "phi")),
+        _ptr(_f32(b, "b")), _ptr(_f32(alpha, "alpha")), T, n, D, iters, eps, _ptr(dx), _ptr(dy),
+        _ptr(dphi), _ptr(db), _ptr(dalpha), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(x.device))
+    _check(st, "mhc_layer_bwd_recompute")
+    if T == 0:  # nothing is written for an empty batch; its gradient is zero
+        for t in (dphi, db, dalpha):
+            t.zero_()
+    return LayerBwdOut(dx, dy, dphi, db, dalpha)
 
 
 def mhc_post_pre(x, y, H_post_l, H_res_l, phi, b, alpha, iters: int = 20,

@@ -250,14 +250,16 @@ cudaError_t launch_pre_cc(bool bf16, const void* x, const float* phi, const floa
         pre_proj_gates_kernel<__nv_bfloat16><<<g1, PT_THREADS, 0, s>>>(
             static_cast<const __nv_bfloat16*>(x), phi, b, alpha, T, D, iters, eps, H_pre, H_post,
             H_res, proj, inv_rms);
-        pre_mix_kernel<__nv_bfloat16><<<g2, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), H_pre, T,
-                                                         D, static_cast<__nv_bfloat16*>(x_in));
+        if (x_in != nullptr)
+            pre_mix_kernel<__nv_bfloat16><<<g2, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), H_pre, T,
+                                                             D, static_cast<__nv_bfloat16*>(x_in));
     } else {
         pre_proj_gates_kernel<float><<<g1, PT_THREADS, 0, s>>>(static_cast<const float*>(x), phi, b, alpha,
                                                                T, D, iters, eps, H_pre, H_post, H_res,
                                                                proj, inv_rms);
-        pre_mix_kernel<float><<<g2, 256, 0, s>>>(static_cast<const float*>(x), H_pre, T, D,
-                                                 static_cast<float*>(x_in));
+        if (x_in != nullptr)
+            pre_mix_kernel<float><<<g2, 256, 0, s>>>(static_cast<const float*>(x), H_pre, T, D,
+                                                     static_cast<float*>(x_in));
     }
     return cudaGetLastError();
 }

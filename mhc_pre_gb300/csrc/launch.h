@@ -30,7 +30,8 @@ struct PreBwdPlan {
 };
 PreBwdPlan pre_bwd_plan(int64_t T, int64_t D);
 
-// Forward (CUDA-core path: projection + gates, then the H_pre mix).
+// Forward (CUDA-core path: projection + gates, then the H_pre mix; no mix
+// when x_in is null).
 cudaError_t launch_pre_cc(bool bf16, const void* x, const float* phi, const float* b,
                           const float* alpha, int64_t T, int64_t D, int iters, float eps,
                           void* x_in, float* H_pre, float* H_post, float* H_res,

@@ -102,6 +102,24 @@ mhc_status mhc_pre(mhc_dtype dt, const void* x, const float* phi, const float* b
                                         H_pre, H_post, H_res, proj, inv_rms, stream));
 }
 
+mhc_status mhc_pre_gates(mhc_dtype dt, const void* x, const float* phi, const float* b,
+                         const float* alpha, int64_t T, int n, int64_t D, int iters, float eps,
+                         float* H_pre, float* H_post, float* H_res, float* proj, float* inv_rms,
+                         cudaStream_t stream) {
+    const void* ptrs[] = {x, phi, b, alpha, H_pre, H_post, H_res, proj, inv_rms};
+    mhc_status st = check_common(dt, T, n, D, ptrs, 9);
+    if (st != MHC_OK) return st;
+    if ((st = check_iters(iters)) != MHC_OK) return st;
+    if (!(eps >= 0.0f) || !isfinite(eps)) return MHC_ERR_INVALID_ARG;
+    if (T == 0) return MHC_OK;
+    // the forward kernels with no x_in buffer skip the mix
+    if (dt == MHC_BF16 && mhc::pre_tc_supports(T, D))
+        return from_cuda(mhc::launch_pre_tc(x, phi, b, alpha, T, D, iters, eps, nullptr, H_pre, H_post,
+                                            H_res, proj, inv_rms, stream));
+    return from_cuda(mhc::launch_pre_cc(dt == MHC_BF16, x, phi, b, alpha, T, D, iters, eps, nullptr,
+                                        H_pre, H_post, H_res, proj, inv_rms, stream));
+}
+
 mhc_status mhc_post(mhc_dtype dt, const void* x, const void* y, const float* H_post,
                     const float* H_res, int64_t T, int n, int64_t D, void* x_next,
                     cudaStream_t stream) {
@@ -199,6 +217,8 @@ int mhc_kernel_launches(const char* op, mhc_dtype dt, int64_t T, int n, int64_t 
         return 1 + (dt == MHC_BF16 && mhc::pre_tc_supports(T, D) ? 1 : 2);
     }
     if (strcmp(op, "mhc_pre_bwd") == 0) return 5;   // both paths: 5 launches
+    if (strcmp(op, "mhc_pre_gates") == 0) return 1;
+    if (strcmp(op, "mhc_layer_bwd_recompute") == 0) return 1 + 1 + 5;
     return -1;
 }
 
@@ -223,6 +243,72 @@ mhc_status mhc_pre_bwd(mhc_dtype dt, const void* g_in, const float* dH_post, con
     return from_cuda(mhc::launch_pre_bwd(dt == MHC_BF16, g_in, dH_post, dH_res, x, phi, b, alpha,
                                          proj, inv_rms, T, D, iters, dx, dphi, db, dalpha,
                                          workspace, stream));
+}
+
+}  // extern "C"
+
+namespace {
+
+// Scratch of mhc_layer_bwd_recompute: the recomputed gates and saved state,
+// the gate gradients, then mhc_pre_bwd's own scratch; 256-byte regions.
+struct RecomputeLayout {
+    size_t H_pre, H_post, H_res, proj, inv_rms, dH_post, dH_res, bwd, total;
+};
+
+RecomputeLayout recompute_layout(int64_t T, int64_t D) {
+    auto r = [](size_t v) { return (v + 255) & ~static_cast<size_t>(255); };
+    const size_t t = static_cast<size_t>(T);
+    RecomputeLayout L;
+    size_t o = 0;
+    L.H_pre = o;   o += r(t * 16);
+    L.H_post = o;  o += r(t * 16);
+    L.H_res = o;   o += r(t * 64);
+    L.proj = o;    o += r(t * 96);
+    L.inv_rms = o; o += r(t * 4);
+    L.dH_post = o; o += r(t * 16);
+    L.dH_res = o;  o += r(t * 64);
+    L.bwd = o;     o += mhc::pre_bwd_plan(T, D).total_bytes;
+    L.total = o;
+    return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mhc_layer_bwd_recompute_workspace_bytes(mhc_dtype dt, int64_t T, int n, int64_t D) {
+    const void* none[] = {nullptr};
+    if (T <= 0 || check_common(dt, T, n, D, none, 0) != MHC_OK) return 0;
+    return recompute_layout(T, D).total;
+}
+
+mhc_status mhc_layer_bwd_recompute(mhc_dtype dt, const void* g_in, const void* g_next, const void* x,
+                                   const void* y, const float* phi, const float* b, const float* alpha,
+                                   int64_t T, int n, int64_t D, int iters, float eps, void* dx, void* dy,
+                                   float* dphi, float* db, float* dalpha, void* workspace, size_t ws_bytes,
+                                   cudaStream_t stream) {
+    const void* ptrs[] = {g_in, g_next, x, y, phi, b, alpha, dx, dy, dphi, db, dalpha, workspace};
+    mhc_status st = check_common(dt, T, n, D, ptrs, 13);
+    if (st != MHC_OK) return st;
+    if ((st = check_iters(iters)) != MHC_OK) return st;
+    if (!(eps >= 0.0f) || !isfinite(eps)) return MHC_ERR_INVALID_ARG;
+    if (T == 0) return MHC_OK;
+    const RecomputeLayout L = recompute_layout(T, D);
+    if (ws_bytes < L.total) return MHC_ERR_INVALID_ARG;
+    unsigned char* w = static_cast<unsigned char*>(workspace);
+    float* H_pre = reinterpret_cast<float*>(w + L.H_pre);
+    float* H_post = reinterpret_cast<float*>(w + L.H_post);
+    float* H_res = reinterpret_cast<float*>(w + L.H_res);
+    float* proj = reinterpret_cast<float*>(w + L.proj);
+    float* inv_rms = reinterpret_cast<float*>(w + L.inv_rms);
+    float* dH_post = reinterpret_cast<float*>(w + L.dH_post);
+    float* dH_res = reinterpret_cast<float*>(w + L.dH_res);
+    st = mhc_pre_gates(dt, x, phi, b, alpha, T, n, D, iters, eps, H_pre, H_post, H_res, proj, inv_rms, stream);
+    if (st != MHC_OK) return st;
+    st = mhc_post_bwd(dt, g_next, x, y, H_post, H_res, T, n, D, dx, dy, dH_post, dH_res, stream);
+    if (st != MHC_OK) return st;
+    return mhc_pre_bwd(dt, g_in, dH_post, dH_res, x, phi, b, alpha, proj, inv_rms, T, n, D, iters, dx, dphi,
+                       db, dalpha, w + L.bwd, ws_bytes - L.bwd, stream);
 }
 
 }  // extern "C"

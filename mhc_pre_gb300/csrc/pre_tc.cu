@@ -4,7 +4,9 @@
 // What it computes, per token (section 5.3 of the "openPangu 2.0 --
 // architecture, training and Ascend systems" notes): inv_rms over the
 // flattened 4*D row, proj = x_bar . phi (24 logits), gates and Sinkhorn, and
-// x_in = sum_i H_pre[i] x[i].
+// x_in = sum_i H_pre[i] x[i].  With no x_in buffer the mix warps only keep
+// the hand-off protocol and the kernel computes the gates and saved state
+// alone (the recompute of the Ascend mHC operator article's backward).
 //
 // Design (GB300, one CTA per SM, persistent):
 //   * A cluster of C CTAs owns a tile of 64 tokens at a time (small tiles keep
@@ -523,7 +525,8 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
             const bool ok = __all_sync(FULL, wait_bar<true>(bar(BAR_HPRE + hs), (it / NHP) & 1, abort_flag));
             const float4* hb = reinterpret_cast<const float4*>(smem + L.hpre) + hs * TILE_M;
             const int qpt = Dc / 8;
-            const int items = ok ? TILE_M * qpt : 0;
+            // no x_in buffer: the gates alone (recompute of the saved state)
+            const int items = (ok && p.x_in != nullptr) ? TILE_M * qpt : 0;
             for (int base = 0; base < items; base += NMIX * 32 * MIX_UNROLL) {
                 uint4 xv[MIX_UNROLL][4];
                 int64_t tok[MIX_UNROLL];

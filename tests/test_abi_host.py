@@ -167,3 +167,45 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(L):
                                  None) == B.MHC_ERR_INVALID_ARG
     assert L.mhc_pre_bwd_noalloc(B.MHC_BF16, *args, 16, 4, 64, 20, MIS, A, A, A,
                                  None) == B.MHC_ERR_MISALIGNED
+
+
+def test_pre_gates_validation(L):
+    def call(dt=B.MHC_BF16, x=A, T=8, n=4, D=64, iters=20, eps=1e-6, outs=None):
+        outs = outs or [A] * 5
+        return L.mhc_pre_gates(dt, x, A, A, A, T, n, D, iters, eps, *outs, None)
+
+    assert call(n=3) == B.MHC_ERR_UNSUPPORTED
+    assert call(D=60) == B.MHC_ERR_UNSUPPORTED
+    assert call(dt=7) == B.MHC_ERR_INVALID_ARG
+    assert call(x=None) == B.MHC_ERR_INVALID_ARG
+    assert call(outs=[A, A, A, MIS, A]) == B.MHC_ERR_MISALIGNED
+    assert call(iters=0) == B.MHC_ERR_INVALID_ARG
+    assert call(eps=float("inf")) == B.MHC_ERR_INVALID_ARG
+    assert L.mhc_pre_gates(B.MHC_BF16, *([None] * 4), 0, 4, 64, 20, 1e-6, *([None] * 5), None) == B.MHC_OK
+    assert L.mhc_kernel_launches(b"mhc_pre_gates", B.MHC_BF16, 8, 4, 64) == 1
+    assert L.mhc_kernel_launches(b"mhc_layer_bwd_recompute", B.MHC_F32, 8, 4, 64) == 7
+
+
+def test_layer_bwd_recompute_workspace_and_validation(L):
+    T, D = 4096, 5120
+    ws = L.mhc_layer_bwd_recompute_workspace_bytes(B.MHC_BF16, T, 4, D)
+    # recomputed gates and saved state (196 B per token) and the gate
+    # gradients (80 B per token) before the pre backward's own scratch
+    assert ws >= T * (196 + 80) + L.mhc_pre_bwd_workspace_bytes(B.MHC_BF16, T, 4, D)
+    assert ws % 16 == 0
+    assert L.mhc_layer_bwd_recompute_workspace_bytes(B.MHC_BF16, 0, 4, D) == 0
+    assert L.mhc_layer_bwd_recompute_workspace_bytes(B.MHC_BF16, T, 3, D) == 0
+
+    def call(T=16, n=4, D=64, iters=20, ws_ptr=A, ws_bytes=None, dx=A):
+        need = L.mhc_layer_bwd_recompute_workspace_bytes(B.MHC_BF16, max(T, 0), 4, D)
+        nb = need if ws_bytes is None else ws_bytes
+        return L.mhc_layer_bwd_recompute(B.MHC_BF16, A, A, A, A, A, A, A, T, n, D, iters, 1e-6,
+                                         dx, A, A, A, A, ws_ptr, nb, None)
+
+    assert call(n=5) == B.MHC_ERR_UNSUPPORTED
+    assert call(ws_ptr=None) == B.MHC_ERR_INVALID_ARG
+    assert call(ws_bytes=1024) == B.MHC_ERR_INVALID_ARG
+    assert call(ws_ptr=MIS) == B.MHC_ERR_MISALIGNED
+    assert call(dx=None) == B.MHC_ERR_INVALID_ARG
+    assert call(iters=B.MAX_ITERS + 1) == B.MHC_ERR_UNSUPPORTED
+    assert call(T=0, ws_ptr=None, dx=None) == B.MHC_OK
