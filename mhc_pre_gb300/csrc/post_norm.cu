@@ -91,6 +91,16 @@ __device__ __forceinline__ float post_elem(const Gates& g, int i, float x0, floa
     return fmaf(g.Hp[i], yv, fmaf(g.H[i][3], x3, fmaf(g.H[i][2], x2, fmaf(g.H[i][1], x1, g.H[i][0] * x0))));
 }
 
+// Asks L2 for a contiguous range ahead of its use (a hint: no data reaches
+// the SM, nothing waits for it).  Pieces of at most 32 KB, 16-byte multiples.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+    const char* c = static_cast<const char*>(p);
+    for (uint32_t off = 0; off < bytes; off += 32768u) {
+        const uint32_t n = bytes - off < 32768u ? bytes - off : 32768u;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(c + off), "r"(n) : "memory");
+    }
+}
+
 template <typename TA, int flags, int PN_THREADS = FWD_NT, int MAXP = FWD_MP>
 __global__ void __launch_bounds__(FWD_NT, FWD_MIN)
 post_norm_kernel(const TA* __restrict__ x, const TA* __restrict__ y, const float* __restrict__ H_post,
@@ -186,6 +196,17 @@ post_norm_bwd_kernel(const TA* __restrict__ g_next, const TA* __restrict__ x, co
         const float s = ((flags & BLOCK) != 0) ? inv_rms_out[t] : 1.0f;
         const TA* xt = x + t * 4 * D;
         const TA* gt = g_next + t * 4 * D;
+        // A token's loads come in dependent steps (the block-norm sum, then
+        // the gradient pass), so have L2 fetch this CTA's next token while
+        // this one works through them: 9% faster with both steps on, and
+        // with neither.  (In the forward the same hint slowed the two-pass
+        // block norm, so it has none.)
+        if (tid == 0 && t + gridDim.x < T) {
+            const int64_t tn = t + gridDim.x;
+            bulk_prefetch_l2(x + tn * 4 * D, static_cast<uint32_t>(4 * D * sizeof(TA)));
+            bulk_prefetch_l2(g_next + tn * 4 * D, static_cast<uint32_t>(4 * D * sizeof(TA)));
+            bulk_prefetch_l2(y + tn * D, static_cast<uint32_t>(D * sizeof(TA)));
+        }
         float yv[MAXP][V];   // y' = y r_y
 #pragma unroll
         for (int k = 0; k < MAXP; ++k) {
