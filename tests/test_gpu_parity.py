@@ -68,6 +68,10 @@ def test_workload4_bf16_fwd_bwd_s4096():
     (1, 4, "f32"), (67, 12, "f32"), (130, 260, "f32"),
     # fewer tokens than one 64-token tile (decode-sized batches)
     (2, 5120, "bf16"), (17, 5120, "bf16"), (63, 2560, "bf16"), (5, 1024, "bf16"),
+    # widths past the cluster kernels' (a phi slice of at most 1280 columns per
+    # CTA): the CUDA-core forward, and the two-pass tensor-core backward from
+    # one 128-token tile up
+    (160, 8192, "bf16"), (33, 8192, "bf16"), (130, 10240, "bf16"),
 ])
 def test_ragged_shapes_fwd_bwd(T, D, dtype):
     w = W.WORKLOADS[4].with_(T=T, D=D, dtype=dtype, wid=40 + T % 50)
