@@ -310,12 +310,13 @@ post_norm_bwd_kernel(const TA* __restrict__ g_next, const TA* __restrict__ x, co
     }
 }
 
-int grid_for(int64_t T) {
+// CTAs per launch: `per_sm` for every SM, at most one per token.
+int grid_for(int64_t T, int per_sm) {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
         n = 148;
-    const int64_t cap = static_cast<int64_t>(n) * 16;
+    const int64_t cap = static_cast<int64_t>(n) * per_sm;
     return static_cast<int>(T < cap ? T : cap);
 }
 
@@ -327,7 +328,7 @@ bool post_norm_supports_impl(bool bf16, int64_t D) {
 template <typename TA, int F>
 void fwd(const void* x, const void* y, const float* H_post, const float* H_res, float eps, int64_t T, int64_t D,
          void* x_next, float* inv_rms_y, float* inv_rms_out, cudaStream_t s) {
-    post_norm_kernel<TA, F><<<grid_for(T), FWD_NT, 0, s>>>(
+    post_norm_kernel<TA, F><<<grid_for(T, 16), FWD_NT, 0, s>>>(
         static_cast<const TA*>(x), static_cast<const TA*>(y), H_post, H_res, eps, T, D, static_cast<TA*>(x_next),
         inv_rms_y, inv_rms_out);
 }
@@ -336,7 +337,9 @@ template <typename TA, int F>
 void bwd(const void* g_next, const void* x, const void* y, const float* H_post, const float* H_res, float eps,
          const float* inv_rms_y, const float* inv_rms_out, int64_t T, int64_t D, void* dx, void* dy,
          float* dH_post, float* dH_res, cudaStream_t s) {
-    post_norm_bwd_kernel<TA, F><<<grid_for(T), BWD_NT, 0, s>>>(
+    // one wave of resident CTAs (two per SM), so that every token after a
+    // CTA's first has been prefetched: 3% faster than 16 per SM with both steps
+    post_norm_bwd_kernel<TA, F><<<grid_for(T, BWD_MIN), BWD_NT, 0, s>>>(
         static_cast<const TA*>(g_next), static_cast<const TA*>(x), static_cast<const TA*>(y), H_post, H_res, eps,
         inv_rms_y, inv_rms_out, T, D, static_cast<TA*>(dx), static_cast<TA*>(dy), dH_post, dH_res);
 }
