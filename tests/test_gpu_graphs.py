@@ -1,7 +1,8 @@
-"""The library's calls inside CUDA graphs: a whole fwd+bwd step, and the
+"""The library's calls inside CUDA graphs: a whole fwd+bwd step, the
 cross-layer step (a memset, a cluster kernel and a second kernel launched
-with programmatic dependent launch), captured once and replayed, give the
-same bits as the same calls run eagerly."""
+with programmatic dependent launch) and the recompute-oriented backward
+(seven launches), captured once and replayed, give the same bits as the same
+calls run eagerly."""
 
 import pytest
 import torch
@@ -57,6 +58,32 @@ def test_cross_layer_step_in_a_cuda_graph_matches_eager():
     gates = W.make_layer_gates(w, device=dev)
     run = lambda: B.mhc_post_pre(a["x"], a["y"], gates["H_post_l"], gates["H_res_l"], a["phi"], a["b"],
                                  a["alpha"], w.iters, w.eps)
+    eager = [t.clone() for t in run()]
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        run()
+    torch.cuda.current_stream(dev).wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        out = run()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert B.get_last_device_error() == B.MHC_OK
+    for e, o in zip(eager, out):
+        assert torch.equal(e, o)
+
+
+def test_recompute_backward_in_a_cuda_graph_matches_eager():
+    dev = _dev()
+    w = W.WORKLOADS[4].with_(T=1000)
+    a = W.make_inputs(w, device=dev)
+    ws = torch.empty((B.layer_bwd_recompute_workspace_bytes(torch.bfloat16, w.T, w.n, w.D),),
+                     dtype=torch.uint8, device=dev)
+    run = lambda: B.mhc_layer_bwd_recompute(a["g_in"], a["g_next"], a["x"], a["y"], a["phi"], a["b"],
+                                            a["alpha"], w.iters, w.eps, workspace=ws)
     eager = [t.clone() for t in run()]
     torch.cuda.synchronize()
     s = torch.cuda.Stream(dev)
