@@ -25,9 +25,11 @@ namespace mhc {
 namespace {
 
 // CTA shapes (threads, 16-byte pieces per thread and row, CTAs per SM), the
-// fastest of those measured at T = 32768, D = 5120 (forward 0.51-0.61 ms,
-// backward 0.85-1.42 ms for flags 0-3; 512 threads x 2 pieces: 0.66-1.0 and
-// 1.2-2.1 ms).  Both cover D <= 8192 (bf16) and 4096 (float32).
+// fastest of those compared at T = 32768, D = 5120 before the backward's
+// prefetch (forward 0.51-0.61 ms, backward 0.85-1.42 ms for flags 0-3;
+// 512 threads x 2 pieces: 0.66-1.0 and 1.2-2.1 ms).  With the prefetch and
+// one wave of CTAs the backward takes 0.77-1.24 ms.  Both cover D <= 8192
+// (bf16) and 4096 (float32).
 constexpr int FWD_NT = 128, FWD_MP = 8, FWD_MIN = 4;
 constexpr int BWD_NT = 256, BWD_MP = 4, BWD_MIN = 2;
 constexpr int MAX_PIECES = 1024;         // NT * MP of both
