@@ -174,31 +174,12 @@ def round_to_storage(v, dtype: str):
     return np.ldexp(np.rint(m * 256.0) / 256.0, e)   # rint: ties to even
 
 
-def fp32_fma(a, b, c):
-    """float32 fused multiply-add, round(a*b + c) once, for float32-valued
-    a, b, c.  The product of two float32 values is exact in float64; the sum
-    is rounded to float64, then to float32 (one rounding, except when the
-    float64 sum lands exactly halfway between two float32 values, a case of
-    probability about 2^-29 per operation)."""
-    return (_f64(a) * _f64(b) + _f64(c)).astype(np.float32).astype(_F)
-
-
 def mhc_post_stored(x, y, H_post, H_res, store: str):
-    """x_next as an activation of type ``store`` holds it.  The pages compute
-    in float32 and store activations in their type; whether a value rounds up
-    or down to bfloat16 is decided in that float32 precision.  The float32 sum
-    runs in stream order, one rounding per multiply-add:
-    x_next[i] = H_post[i] y + (H_res[i,3] x[3] + (H_res[i,2] x[2]
-                + (H_res[i,1] x[1] + H_res[i,0] x[0])))."""
-    x = _f64(x)
-    Hr = _f64(H_res).astype(np.float32).astype(_F)
-    Hp = _f64(H_post).astype(np.float32).astype(_F)
-    n = x.shape[1]
-    acc = (Hr[:, :, 0, None] * x[:, None, 0, :]).astype(np.float32).astype(_F)
-    for j in range(1, n):
-        acc = fp32_fma(Hr[:, :, j, None], x[:, None, j, :], acc)
-    acc = fp32_fma(Hp[:, :, None], _f64(y)[:, None, :], acc)
-    return round_to_storage(acc, store)
+    """x_next as an activation of type ``store`` holds it: the exact update
+    rounded once to that type.  The pages compute in float32 and store each
+    activation in its own type; they fix no order for the float32 sum, so
+    the plainest reading is the exact value, rounded once at the store."""
+    return round_to_storage(mhc_post(x, y, H_post, H_res), store)
 
 
 def mhc_post_pre(x, y, H_post_l, H_res_l, phi, b, alpha, iters: int, eps: float,
