@@ -26,7 +26,8 @@
  *     Activations (x, y, x_in, x_next, g_in, g_next, dx, dy) have type `dt`;
  *     gates, phi, b, alpha, saved state and parameter gradients are float32.
  *   - Every pointer must be 16-byte aligned.  n must be 4.  D must be a
- *     multiple of 8 (bf16) or 4 (float32).  T = 0 is a no-op.
+ *     multiple of 8 (bf16) or 4 (float32).  T = 0 launches no kernel; the
+ *     backward entry points then write zero parameter gradients (below).
  *   - Calls are asynchronous on `stream` (0 = legacy default stream) and
  *     never synchronise the host.  A bad argument returns an error before
  *     anything is launched; a failed launch returns MHC_ERR_CUDA.  Errors that
@@ -225,9 +226,11 @@ size_t mhc_pre_bwd_workspace_bytes(mhc_dtype dt, int64_t T, int n, int64_t D);
  *
  * Data parallelism: dphi, db and dalpha are sums over this call's tokens, so
  * ranks that each hold a slice of the batch add them (one all-reduce) to get
- * the full-batch gradient; every other output is per token.  For T = 0
- * nothing is written, not even dphi, db and dalpha: a caller that takes part
- * in such a sum with no tokens sets them to zero itself.
+ * the full-batch gradient; every other output is per token.  For T = 0 the
+ * call writes zero parameter gradients (dphi, db and dalpha, the sums over no
+ * tokens, with memsets on `stream`), so a rank with no tokens contributes
+ * zero to that sum; the per-token pointers may then be null, dphi, db and
+ * dalpha may not.
  */
 mhc_status mhc_pre_bwd(mhc_dtype dt, const void* g_in, const float* dH_post,
                        const float* dH_res, const void* x, const float* phi,
@@ -259,12 +262,15 @@ mhc_status mhc_pre_bwd(mhc_dtype dt, const void* g_in, const float* dH_post,
  *     MHC_ERR_UNSUPPORTED when T * 256 bytes of per-token records, one
  *     4*D x 24 float32 partial of dphi and D * 256 bytes of bf16 phi blocks
  *     exceed it (for D = 5120: T <= 52,736).
- *   - The first call on a device looks up the array's device address on that
- *     device (cudaGetSymbolAddress); make that first call before any stream
- *     capture.
+ *   - The first call in each CUDA context looks up the array's device address
+ *     in that context (cudaGetSymbolAddress) and keeps it for that context;
+ *     a context created later (for example after cudaDeviceReset) gets a
+ *     lookup of its own.  That first call must not come while `stream` is
+ *     being captured: it then returns MHC_ERR_UNSUPPORTED and does nothing.
  *   - All calls share the array; calls that overlap on the GPU race on it.
  *     Every element is written before it is read, so no state carries over
  *     from one call to the next.
+ *   - T = 0 writes zero parameter gradients, as mhc_pre_bwd.
  */
 mhc_status mhc_pre_bwd_noalloc(mhc_dtype dt, const void* g_in, const float* dH_post,
                                const float* dH_res, const void* x, const float* phi,
@@ -327,7 +333,8 @@ size_t mhc_layer_bwd_recompute_workspace_bytes(mhc_dtype dt, int64_t T, int n,
  *   workspace, ws_bytes        device scratch of at least
  *                              mhc_layer_bwd_recompute_workspace_bytes() bytes
  * Errors as mhc_pre_bwd; MHC_ERR_INVALID_ARG for a missing or short
- * workspace.  Data parallelism as mhc_pre_bwd.
+ * workspace.  Data parallelism and T = 0 (zero dphi, db, dalpha) as
+ * mhc_pre_bwd.
  */
 mhc_status mhc_layer_bwd_recompute(mhc_dtype dt, const void* g_in, const void* g_next,
                                    const void* x, const void* y, const float* phi,

@@ -199,9 +199,6 @@ def mhc_layer_bwd_recompute(g_in, g_next, x, y, phi, b, alpha, iters: int = 20,
         _ptr(dphi), _ptr(db), _ptr(dalpha), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(x.device))
     _check(st, "mhc_layer_bwd_recompute")
-    if T == 0:  # nothing is written for an empty batch; its gradient is zero
-        for t in (dphi, db, dalpha):
-            t.zero_()
     return LayerBwdOut(dx, dy, dphi, db, dalpha)
 
 
@@ -317,9 +314,6 @@ def mhc_pre_bwd(g_in, dH_post, dH_res, x, phi, b, alpha, proj, inv_rms, dx,
                            _ptr(workspace), workspace.numel() * workspace.element_size(),
                            _stream(x.device))
     _check(st, "mhc_pre_bwd")
-    if T == 0:  # the library writes nothing for an empty batch; its gradient is zero
-        for t in (dphi, db, dalpha):
-            t.zero_()
     return PreBwdOut(dx, dphi, db, dalpha)
 
 
@@ -343,9 +337,6 @@ def mhc_pre_bwd_noalloc(g_in, dH_post, dH_res, x, phi, b, alpha, proj, inv_rms,
         _ptr(_f32(proj, "proj")), _ptr(_f32(inv_rms, "inv_rms")), T, n, D, iters, _ptr(dx),
         _ptr(dphi), _ptr(db), _ptr(dalpha), _stream(x.device))
     _check(st, "mhc_pre_bwd_noalloc")
-    if T == 0:
-        for t in (dphi, db, dalpha):
-            t.zero_()
     return PreBwdOut(dx, dphi, db, dalpha)
 
 

@@ -30,6 +30,10 @@ struct PreBwdPlan {
 };
 PreBwdPlan pre_bwd_plan(int64_t T, int64_t D);
 
+// The gradients of phi [4D, 24], b [24] and alpha [3] of an empty batch: sums
+// over no tokens, so zero.  Writes them with three memsets on `s`.
+cudaError_t zero_param_grads(int64_t D, float* dphi, float* db, float* dalpha, cudaStream_t s);
+
 // Forward (CUDA-core path: projection + gates, then the H_pre mix; no mix
 // when x_in is null).
 cudaError_t launch_pre_cc(bool bf16, const void* x, const float* phi, const float* b,

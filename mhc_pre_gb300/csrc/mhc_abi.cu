@@ -42,7 +42,24 @@ mhc_status check_iters(int iters) {
 
 mhc_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA; }
 
+// The parameter gradients of an empty batch (T = 0): every other pointer may
+// be null then, these three must be valid.
+mhc_status empty_batch_param_grads(int64_t D, float* dphi, float* db, float* dalpha, cudaStream_t s) {
+    if (dphi == nullptr || db == nullptr || dalpha == nullptr) return MHC_ERR_INVALID_ARG;
+    if (!aligned16(dphi) || !aligned16(db) || !aligned16(dalpha)) return MHC_ERR_MISALIGNED;
+    return from_cuda(mhc::zero_param_grads(D, dphi, db, dalpha, s));
+}
+
 }  // namespace
+
+namespace mhc {
+cudaError_t zero_param_grads(int64_t D, float* dphi, float* db, float* dalpha, cudaStream_t s) {
+    cudaError_t e = cudaMemsetAsync(dphi, 0, static_cast<size_t>(4 * D) * 24 * sizeof(float), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(db, 0, 24 * sizeof(float), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dalpha, 0, 3 * sizeof(float), s);
+    return e;
+}
+}  // namespace mhc
 
 namespace mhc {
 // Defined in pre_tc.cu: the tensor-core pre forward (bf16).  Returns
@@ -238,7 +255,7 @@ mhc_status mhc_pre_bwd(mhc_dtype dt, const void* g_in, const float* dH_post, con
     mhc_status st = check_common(dt, T, n, D, ptrs, 14);
     if (st != MHC_OK) return st;
     if ((st = check_iters(iters)) != MHC_OK) return st;
-    if (T == 0) return MHC_OK;
+    if (T == 0) return empty_batch_param_grads(D, dphi, db, dalpha, stream);
     if (ws_bytes < mhc::pre_bwd_plan(T, D).total_bytes) return MHC_ERR_INVALID_ARG;
     return from_cuda(mhc::launch_pre_bwd(dt == MHC_BF16, g_in, dH_post, dH_res, x, phi, b, alpha,
                                          proj, inv_rms, T, D, iters, dx, dphi, db, dalpha,
@@ -292,7 +309,7 @@ mhc_status mhc_layer_bwd_recompute(mhc_dtype dt, const void* g_in, const void* g
     if (st != MHC_OK) return st;
     if ((st = check_iters(iters)) != MHC_OK) return st;
     if (!(eps >= 0.0f) || !isfinite(eps)) return MHC_ERR_INVALID_ARG;
-    if (T == 0) return MHC_OK;
+    if (T == 0) return empty_batch_param_grads(D, dphi, db, dalpha, stream);
     const RecomputeLayout L = recompute_layout(T, D);
     if (ws_bytes < L.total) return MHC_ERR_INVALID_ARG;
     unsigned char* w = static_cast<unsigned char*>(workspace);

@@ -12,12 +12,18 @@
 // The array is a file-scope __device__ variable, so every GPU that loads the
 // library holds it (MHC_PRE_BWD_NOALLOC_SCRATCH_BYTES) until the process
 // exits.  In host code its name is only a host-side stand-in, never a device
-// address: the device address is fetched with cudaGetSymbolAddress once per
-// device (with that device current) on the first call on that device, and
-// passed to the kernels.  All calls share the array and it keeps the last
-// call's contents; every kernel here writes each scratch element before it
-// reads it, so nothing needs clearing.  Calls that overlap on the GPU (for
-// example on two streams of one device) race on the array.
+// address: the device address is fetched with cudaGetSymbolAddress, with the
+// device current, on the first call in each CUDA context, and passed to the
+// kernels.  The cache is keyed by the context's unique id, so a context
+// created later on the same device (after cudaDeviceReset, or a non-primary
+// context) gets its own lookup.  A first call in a context made while its
+// stream is being captured returns MHC_ERR_UNSUPPORTED instead of looking the
+// address up.  All calls share the array and it keeps the last call's
+// contents; every kernel here writes each scratch element before it reads it,
+// so nothing needs clearing.  Calls that overlap on the GPU (for example on
+// two streams of one device) race on the array.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "../../include/mhc.h"
@@ -30,23 +36,79 @@ static __device__ __align__(256) unsigned char g_pre_bwd_scratch[MHC_PRE_BWD_NOA
 namespace {
 
 constexpr int kLogits = 24;   // 2n + n^2 gate logits for n = 4
-constexpr int kMaxDevices = 64;
-std::mutex g_setup_mutex;
-void* g_scratch_ptr[kMaxDevices];
+constexpr int kMaxContexts = 64;
 
-// Device address of the scratch array on the current device (set up once per
-// device).  Returns nullptr if the device cannot be queried or the symbol
-// cannot be resolved.
-void* scratch_on_current_device() {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
-        void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_pre_bwd_scratch) != cudaSuccess) return nullptr;
-        g_scratch_ptr[dev] = ptr;
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+std::mutex g_setup_mutex;
+struct Entry {
+    unsigned long long ctx_id;
+    void* ptr;
+};
+Entry g_cache[kMaxContexts];
+int g_ncache = 0;
+
+// Unique id of the calling thread's current context (0 if there is none or
+// the driver entry points are unavailable).
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(f);
+    });
+    if (get_current == nullptr || get_id == nullptr) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Device address of the scratch array in the current context, looked up on
+// the first call in that context.  `status` is MHC_ERR_UNSUPPORTED when that
+// first call comes while `stream` is capturing, MHC_ERR_CUDA when the context
+// or the symbol cannot be resolved.
+void* scratch_in_current_context(cudaStream_t stream, mhc_status* status) {
+    unsigned long long id = current_context_id();
+    if (id == 0) {
+        // no context is current on this thread yet: make the current device's
+        // primary context current (cudaSetDevice initialises it)
+        int dev = -1;
+        if (cudaGetDevice(&dev) == cudaSuccess && cudaSetDevice(dev) == cudaSuccess) id = current_context_id();
     }
-    return g_scratch_ptr[dev];
+    if (id == 0) {
+        *status = MHC_ERR_CUDA;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    for (int i = 0; i < g_ncache; ++i)
+        if (g_cache[i].ctx_id == id) return g_cache[i].ptr;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+        *status = MHC_ERR_CUDA;
+        return nullptr;
+    }
+    if (cap != cudaStreamCaptureStatusNone) {
+        *status = MHC_ERR_UNSUPPORTED;
+        return nullptr;
+    }
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_pre_bwd_scratch) != cudaSuccess || ptr == nullptr) {
+        *status = MHC_ERR_CUDA;
+        return nullptr;
+    }
+    if (g_ncache < kMaxContexts) g_cache[g_ncache++] = Entry{id, ptr};
+    return ptr;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -67,7 +129,15 @@ extern "C" mhc_status mhc_pre_bwd_noalloc(mhc_dtype dt, const void* g_in, const 
     if (T > (int64_t(1) << 31) || D > (int64_t(1) << 24)) return MHC_ERR_UNSUPPORTED;
     if (iters < 1) return MHC_ERR_INVALID_ARG;
     if (iters > MHC_MAX_ITERS) return MHC_ERR_UNSUPPORTED;
-    if (T == 0) return MHC_OK;
+    if (T == 0) {
+        // the parameter gradients of an empty batch are zero
+        const void* out[] = {dphi, db, dalpha};
+        for (const void* p : out) {
+            if (p == nullptr) return MHC_ERR_INVALID_ARG;
+            if (!mhc::aligned16(p)) return MHC_ERR_MISALIGNED;
+        }
+        return mhc::zero_param_grads(D, dphi, db, dalpha, stream) == cudaSuccess ? MHC_OK : MHC_ERR_CUDA;
+    }
     const void* ptrs[] = {g_in, dH_post, dH_res, x, phi, b, alpha, proj, inv_rms, dx, dphi, db, dalpha};
     for (const void* p : ptrs) {
         if (p == nullptr) return MHC_ERR_INVALID_ARG;
@@ -84,8 +154,9 @@ extern "C" mhc_status mhc_pre_bwd_noalloc(mhc_dtype dt, const void* g_in, const 
     int64_t nb = mhc::pre_bwd_plan(T, D).nb;
     const int64_t fit = static_cast<int64_t>((cap - rec_bytes - phi_bytes) / part_bytes);
     if (nb > fit) nb = fit;
-    void* ws = mhc::scratch_on_current_device();
-    if (ws == nullptr) return MHC_ERR_CUDA;
+    mhc_status st = MHC_OK;
+    void* ws = mhc::scratch_in_current_context(stream, &st);
+    if (ws == nullptr) return st;
     const cudaError_t e = mhc::launch_pre_bwd_blocks(dt == MHC_BF16, g_in, dH_post, dH_res, x, phi, b,
                                                      alpha, proj, inv_rms, T, D, iters, dx, dphi, db,
                                                      dalpha, ws, nb, stream);

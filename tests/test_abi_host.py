@@ -1,8 +1,11 @@
 """Host-side checks of the C-ABI library: it loads, exports every function
 ``include/mhc.h`` declares, and rejects bad arguments before any launch.
 
-No call here reaches the GPU: every argument set is refused (or is the T = 0
-no-op) by host validation, which runs before any CUDA call.
+No call here reaches the GPU: every argument set is refused by host
+validation, which runs before any CUDA call, or is a T = 0 call that launches
+nothing and writes nothing.  (For T = 0 the backward entry points write zero
+parameter gradients; with fake addresses those calls are only checked for
+their refusals here, and tests/test_gpu_parity.py checks the zeros on a GPU.)
 """
 
 import ctypes
@@ -123,11 +126,11 @@ def test_pre_bwd_workspace_and_validation(L):
     assert L.mhc_pre_bwd_workspace_bytes(B.MHC_BF16, 0, 4, 5120) == 0
     assert L.mhc_pre_bwd_workspace_bytes(B.MHC_BF16, 16, 3, 5120) == 0
 
-    def call(T=16, n=4, D=64, iters=20, ws_ptr=A, ws_bytes=None, dx=A):
+    def call(T=16, n=4, D=64, iters=20, ws_ptr=A, ws_bytes=None, dx=A, dphi=A):
         need = L.mhc_pre_bwd_workspace_bytes(B.MHC_BF16, max(T, 0), 4, D)
         wb = need if ws_bytes is None else ws_bytes
         return L.mhc_pre_bwd(B.MHC_BF16, A, A, A, A, A, A, A, A, A, T, n, D, iters,
-                             dx, A, A, A, ws_ptr, wb, None)
+                             dx, dphi, A, A, ws_ptr, wb, None)
 
     assert call(n=5) == B.MHC_ERR_UNSUPPORTED
     assert call(iters=0) == B.MHC_ERR_INVALID_ARG
@@ -136,7 +139,9 @@ def test_pre_bwd_workspace_and_validation(L):
     assert call(dx=MIS) == B.MHC_ERR_MISALIGNED
     need = L.mhc_pre_bwd_workspace_bytes(B.MHC_BF16, 16, 4, 64)
     assert call(ws_bytes=need - 16) == B.MHC_ERR_INVALID_ARG
-    assert call(T=0, ws_ptr=None, ws_bytes=0) == B.MHC_OK
+    # T = 0 writes zero parameter gradients: their pointers must be valid
+    assert call(T=0, ws_ptr=None, ws_bytes=0, dx=None, dphi=None) == B.MHC_ERR_INVALID_ARG
+    assert call(T=0, ws_ptr=None, ws_bytes=0, dx=None, dphi=MIS) == B.MHC_ERR_MISALIGNED
 
 
 def test_binding_refuses_cpu_tensors():
@@ -162,7 +167,11 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(L):
 
     assert call(60000, 5120) == B.MHC_ERR_UNSUPPORTED
     assert call(1 << 20, 64) == B.MHC_ERR_UNSUPPORTED
-    assert call(0, 5120) == B.MHC_OK
+    # T = 0 writes zero parameter gradients: their pointers must be valid
+    assert L.mhc_pre_bwd_noalloc(B.MHC_BF16, *args, 0, 4, 5120, 20, None, None, A, A,
+                                 None) == B.MHC_ERR_INVALID_ARG
+    assert L.mhc_pre_bwd_noalloc(B.MHC_BF16, *args, 0, 4, 5120, 20, None, A, MIS, A,
+                                 None) == B.MHC_ERR_MISALIGNED
     assert L.mhc_pre_bwd_noalloc(B.MHC_BF16, *args, 16, 4, 64, 0, A, A, A, A,
                                  None) == B.MHC_ERR_INVALID_ARG
     assert L.mhc_pre_bwd_noalloc(B.MHC_BF16, *args, 16, 4, 64, 20, MIS, A, A, A,
@@ -196,11 +205,11 @@ def test_layer_bwd_recompute_workspace_and_validation(L):
     assert L.mhc_layer_bwd_recompute_workspace_bytes(B.MHC_BF16, 0, 4, D) == 0
     assert L.mhc_layer_bwd_recompute_workspace_bytes(B.MHC_BF16, T, 3, D) == 0
 
-    def call(T=16, n=4, D=64, iters=20, ws_ptr=A, ws_bytes=None, dx=A):
+    def call(T=16, n=4, D=64, iters=20, ws_ptr=A, ws_bytes=None, dx=A, dphi=A):
         need = L.mhc_layer_bwd_recompute_workspace_bytes(B.MHC_BF16, max(T, 0), 4, D)
         nb = need if ws_bytes is None else ws_bytes
         return L.mhc_layer_bwd_recompute(B.MHC_BF16, A, A, A, A, A, A, A, T, n, D, iters, 1e-6,
-                                         dx, A, A, A, A, ws_ptr, nb, None)
+                                         dx, A, dphi, A, A, ws_ptr, nb, None)
 
     assert call(n=5) == B.MHC_ERR_UNSUPPORTED
     assert call(ws_ptr=None) == B.MHC_ERR_INVALID_ARG
@@ -208,4 +217,5 @@ def test_layer_bwd_recompute_workspace_and_validation(L):
     assert call(ws_ptr=MIS) == B.MHC_ERR_MISALIGNED
     assert call(dx=None) == B.MHC_ERR_INVALID_ARG
     assert call(iters=B.MAX_ITERS + 1) == B.MHC_ERR_UNSUPPORTED
-    assert call(T=0, ws_ptr=None, dx=None) == B.MHC_OK
+    assert call(T=0, ws_ptr=None, dx=None, dphi=None) == B.MHC_ERR_INVALID_ARG
+    assert call(T=0, ws_ptr=None, dx=None, dphi=MIS) == B.MHC_ERR_MISALIGNED

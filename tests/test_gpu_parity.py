@@ -110,15 +110,37 @@ def test_empty_batch_is_a_noop():
     assert f.x_in.shape == (0, 64)
     xn = B.mhc_post(x, torch.empty((0, 64), dtype=torch.bfloat16, device=dev), f.H_post, f.H_res)
     assert xn.shape == (0, 4, 64)
-    # an empty batch contributes zero parameter gradient (a data-parallel rank
-    # with no tokens still takes part in the sum)
-    e = torch.empty((0, 4), device=dev)
-    qb = B.mhc_pre_bwd(torch.empty((0, 64), dtype=torch.bfloat16, device=dev), e,
-                       torch.empty((0, 4, 4), device=dev), x, phi, torch.zeros(24, device=dev),
-                       torch.zeros(3, device=dev), torch.empty((0, 24), device=dev),
-                       torch.empty((0,), device=dev), torch.empty_like(x))
-    for t in (qb.dphi, qb.db, qb.dalpha):
-        assert torch.count_nonzero(t).item() == 0
+
+
+def test_empty_batch_writes_zero_param_grads():
+    """An empty batch contributes zero parameter gradient (a data-parallel rank
+    with no tokens still takes part in the sum): each backward entry point
+    writes the zeros itself, through the C ABI, over buffers that start as NaN."""
+    dev = _dev()
+    L = B.lib()
+    D = 64
+    s = torch.cuda.current_stream().cuda_stream
+
+    def grads():
+        return [torch.full((4 * D, 24), float("nan"), device=dev), torch.full((24,), float("nan"), device=dev),
+                torch.full((3,), float("nan"), device=dev)]
+
+    g = grads()
+    assert L.mhc_pre_bwd(B.MHC_BF16, *([None] * 9), 0, 4, D, 20, None, *[t.data_ptr() for t in g],
+                         None, 0, s) == B.MHC_OK
+    torch.cuda.synchronize()
+    assert all(torch.count_nonzero(t).item() == 0 for t in g)
+    g = grads()
+    assert L.mhc_pre_bwd_noalloc(B.MHC_BF16, *([None] * 9), 0, 4, D, 20, None,
+                                 *[t.data_ptr() for t in g], s) == B.MHC_OK
+    torch.cuda.synchronize()
+    assert all(torch.count_nonzero(t).item() == 0 for t in g)
+    g = grads()
+    assert L.mhc_layer_bwd_recompute(B.MHC_F32, *([None] * 7), 0, 4, D, 20, 1e-6, None, None,
+                                     *[t.data_ptr() for t in g], None, 0, s) == B.MHC_OK
+    torch.cuda.synchronize()
+    assert all(torch.count_nonzero(t).item() == 0 for t in g)
+    assert B.get_last_device_error() == B.MHC_OK
 
 
 def test_invariants_hold_on_gpu_output():
