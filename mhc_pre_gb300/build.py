@@ -18,7 +18,8 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmhc_gb300.so")
 
-SOURCES = ["mhc_abi.cu", "kernels_fwd.cu", "kernels_bwd.cu", "pre_tc.cu", "pre_bwd_tc.cu", "pre_bwd_fused.cu",
+SOURCES = ["mhc_abi.cu", "kernels_fwd.cu", "kernels_bwd.cu", "pre_tc.cu", "pre_bwd_tc.cu",
+           "pre_bwd_fused.cu",
            "pre_bwd_noalloc.cu", "post_pre_tc.cu",
            "post_norm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -225,7 +225,8 @@ int mhc_kernel_launches(const char* op, mhc_dtype dt, int64_t T, int n, int64_t 
     const void* none[] = {nullptr};
     if (check_common(dt, T, n, D, none, 0) != MHC_OK) return -1;
     if (T == 0) return 0;
-    if (strcmp(op, "mhc_pre") == 0) return dt == MHC_BF16 && mhc::pre_tc_supports(T, D) ? 1 : 2;
+    if (strcmp(op, "mhc_pre") == 0)
+        return dt == MHC_BF16 && mhc::pre_tc_supports(T, D) ? 1 : 2;
     if (strcmp(op, "mhc_post") == 0 || strcmp(op, "mhc_post_bwd") == 0) return 1;
     if (strcmp(op, "mhc_post_norm") == 0 || strcmp(op, "mhc_post_norm_bwd") == 0)
         return mhc::post_norm_supports(dt == MHC_BF16, D) ? 1 : -1;

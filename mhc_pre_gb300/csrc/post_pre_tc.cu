@@ -419,7 +419,8 @@ post_pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
                 if (lane == 0) ptx::mbar_arrive(bar(BAR_SKFULL + tb));
                 if (lane == 0 && it + 1 < ntl) ptx::mbar_arrive_expect_tx(bar(BAR_RECV), 2 * TILE_M * REC_TX);
                 __syncwarp();
-                if (lane < C) ptx::mbar_arrive_remote(ptx::mapa(bar(BAR_RFREE), static_cast<uint32_t>(lane)));
+                // a credit: the records read above already feed the sums
+                if (lane < C) ptx::mbar_arrive_remote_relaxed(ptx::mapa(bar(BAR_RFREE), static_cast<uint32_t>(lane)));
             }
         }
     } else if (warp == SK_WARP) {

@@ -475,8 +475,8 @@ pre_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
             }
             if (ptx::named_bar_or(2, NPREP * 32, !ok)) goto done;
             if (t < static_cast<int>(C)) {
-                ptx::fence_acq_rel_cluster();
-                ptx::mbar_arrive_remote(ptx::mapa(bar(BAR_PEMPTY + ps), static_cast<uint32_t>(t)));
+                // a credit: the partials read above already feed dh
+                ptx::mbar_arrive_remote_relaxed(ptx::mapa(bar(BAR_PEMPTY + ps), static_cast<uint32_t>(t)));
             }
             float dl[4], cadd = 0.f, da0 = 0.f;
 #pragma unroll

@@ -456,7 +456,11 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
                 if (lane == 0) ptx::mbar_arrive(bar(BAR_SKFULL + tb));
                 if (lane == 0 && it + 1 < ntl) ptx::mbar_arrive_expect_tx(bar(BAR_RECV), 2 * TILE_M * REC_TX);
                 __syncwarp();
-                if (lane < C) ptx::mbar_arrive_remote(ptx::mapa(bar(BAR_RFREE), static_cast<uint32_t>(lane)));
+                // a credit: every record value read above already feeds this
+                // warp's sums, so a relaxed arrive suffices (a cluster-scope
+                // release would wait about a microsecond for the SM's
+                // outstanding memory operations)
+                if (lane < C) ptx::mbar_arrive_remote_relaxed(ptx::mapa(bar(BAR_RFREE), static_cast<uint32_t>(lane)));
             }
         }
     } else if (warp == SK_WARP) {
@@ -568,7 +572,9 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
             if (warp == MIX_WARP0) {
                 if (lane == 0 && it + NHP < ntl) ptx::mbar_arrive_expect_tx(bar(BAR_HPRE + hs), TILE_M * 16);
                 __syncwarp();
-                if (lane < C) ptx::mbar_arrive_remote(ptx::mapa(bar(BAR_HFREE + hs), static_cast<uint32_t>(lane)));
+                // a credit: the H_pre values read from the buffer were used by
+                // every mix thread before the named barrier above
+                if (lane < C) ptx::mbar_arrive_remote_relaxed(ptx::mapa(bar(BAR_HFREE + hs), static_cast<uint32_t>(lane)));
             }
         }
     }

@@ -38,6 +38,14 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cbar) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar)
                  : "memory");
 }
+// Relaxed arrive on a barrier of another CTA of the cluster: no release
+// fence (a cluster-scope release waits for the SM's outstanding memory
+// operations, about a microsecond under load).  For credits whose reads are
+// complete before the arrive: their values already feed this thread's
+// arithmetic.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cbar) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -284,7 +292,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
-
 // Shared-memory matrix descriptor of a K-major operand stored with the
 // 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.  The
 // tile base must be 1024-byte aligned; a K offset inside the 128-byte row is
