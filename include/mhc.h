@@ -193,6 +193,20 @@ mhc_status mhc_post_bwd(mhc_dtype dt, const void* g_next, const void* x,
                         int64_t T, int n, int64_t D, void* dx, void* dy,
                         float* dH_post, float* dH_res, cudaStream_t stream);
 
+/*
+ * mhc_test_force_timeout -- test hook of the failure path, off by default.
+ * While on (nonzero), every launch of the bf16 tensor-core forward kernel
+ * (mhc_pre, mhc_pre_gates) and of the pre backward's one-pass cluster kernel
+ * (mhc_pre_bwd) makes thread 0 of each CTA wait on an mbarrier that nothing
+ * arrives on; the wait gives up after about 100 us, the kernel latches its
+ * device error word and returns before starting any copy or tensor-memory
+ * allocation, leaving its outputs unwritten.  The next
+ * mhc_get_last_device_error() then reports MHC_ERR_TIMEOUT, and the context
+ * stays usable.  Synchronous (it writes a device flag); applies to the
+ * current device.  Not for production use.
+ */
+mhc_status mhc_test_force_timeout(int on);
+
 /* Number of kernels the entry point `op` ("mhc_pre", "mhc_pre_gates",
  * "mhc_post", "mhc_post_norm", "mhc_post_norm_bwd", "mhc_post_pre",
  * "mhc_post_bwd", "mhc_pre_bwd" or "mhc_layer_bwd_recompute") launches for these sizes; -1 for an

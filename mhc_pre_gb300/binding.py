@@ -30,7 +30,7 @@ EXPORTS = ("mhc_status_string", "mhc_version", "mhc_get_last_device_error",
            "mhc_post_bwd", "mhc_kernel_launches",
            "mhc_pre_bwd_workspace_bytes", "mhc_pre_bwd", "mhc_pre_bwd_noalloc",
            "mhc_pre_gates", "mhc_layer_bwd_recompute_workspace_bytes",
-           "mhc_layer_bwd_recompute")
+           "mhc_layer_bwd_recompute", "mhc_test_force_timeout")
 
 PreOut = namedtuple("PreOut", "x_in H_pre H_post H_res proj inv_rms")
 PostPreOut = namedtuple("PostPreOut", "x_next x_in H_pre H_post H_res proj inv_rms")
@@ -66,11 +66,19 @@ _SIGS = {
     "mhc_pre_gates": ([_I, _P, _P, _P, _P, _I64, _I, _I64, _I, _F,
                        _P, _P, _P, _P, _P, _P], _I),
     "mhc_layer_bwd_recompute_workspace_bytes": ([_I, _I64, _I, _I64], ctypes.c_size_t),
+    "mhc_test_force_timeout": ([_I], _I),
     "mhc_layer_bwd_recompute": ([_I, _P, _P, _P, _P, _P, _P, _P, _I64, _I, _I64, _I, _F,
                                  _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P], _I),
 }
 
 _lib = None
+
+
+def _empty(shape, dtype=None, device=None):
+    """Allocates every output and workspace buffer this module hands to the
+    library.  Plain torch.empty; the guard-band tests put an allocator that
+    surrounds each buffer with sentinel bytes in its place."""
+    return torch.empty(shape, dtype=dtype, device=device)
 
 
 class MhcError(RuntimeError):
@@ -144,10 +152,10 @@ def mhc_pre(x, phi, b, alpha, iters: int = 20, eps: float = 1e-6):
     T, n, D = x.shape
     G = 2 * n + n * n
     f32 = dict(dtype=torch.float32, device=x.device)
-    out = PreOut(torch.empty((T, D), dtype=x.dtype, device=x.device),
-                 torch.empty((T, n), **f32), torch.empty((T, n), **f32),
-                 torch.empty((T, n, n), **f32), torch.empty((T, G), **f32),
-                 torch.empty((T,), **f32))
+    out = PreOut(_empty((T, D), dtype=x.dtype, device=x.device),
+                 _empty((T, n), **f32), _empty((T, n), **f32),
+                 _empty((T, n, n), **f32), _empty((T, G), **f32),
+                 _empty((T,), **f32))
     st = lib().mhc_pre(_dtype_code(x), _ptr(x), _ptr(_f32(phi, "phi")),
                        _ptr(_f32(b, "b")), _ptr(_f32(alpha, "alpha")), T, n, D,
                        iters, eps, *[_ptr(o) for o in out], _stream(x.device))
@@ -161,9 +169,9 @@ def mhc_pre_gates(x, phi, b, alpha, iters: int = 20, eps: float = 1e-6):
     T, n, D = x.shape
     G = 2 * n + n * n
     f32 = dict(dtype=torch.float32, device=x.device)
-    out = PreGatesOut(torch.empty((T, n), **f32), torch.empty((T, n), **f32),
-                      torch.empty((T, n, n), **f32), torch.empty((T, G), **f32),
-                      torch.empty((T,), **f32))
+    out = PreGatesOut(_empty((T, n), **f32), _empty((T, n), **f32),
+                      _empty((T, n, n), **f32), _empty((T, G), **f32),
+                      _empty((T,), **f32))
     st = lib().mhc_pre_gates(_dtype_code(x), _ptr(x), _ptr(_f32(phi, "phi")),
                              _ptr(_f32(b, "b")), _ptr(_f32(alpha, "alpha")), T, n, D,
                              iters, eps, *[_ptr(o) for o in out], _stream(x.device))
@@ -186,13 +194,13 @@ def mhc_layer_bwd_recompute(g_in, g_next, x, y, phi, b, alpha, iters: int = 20,
         raise TypeError("g_in, g_next, x and y must share a dtype")
     need = layer_bwd_recompute_workspace_bytes(x.dtype, T, n, D)
     if workspace is None:
-        workspace = torch.empty((max(need, 16),), dtype=torch.uint8, device=x.device)
+        workspace = _empty((max(need, 16),), dtype=torch.uint8, device=x.device)
     f32 = dict(dtype=torch.float32, device=x.device)
-    dx = torch.empty_like(x)
-    dy = torch.empty_like(y)
-    dphi = torch.empty((n * D, G), **f32)
-    db = torch.empty((G,), **f32)
-    dalpha = torch.empty((3,), **f32)
+    dx = _empty(x.shape, x.dtype, x.device)
+    dy = _empty(y.shape, y.dtype, y.device)
+    dphi = _empty((n * D, G), **f32)
+    db = _empty((G,), **f32)
+    dalpha = _empty((3,), **f32)
     st = lib().mhc_layer_bwd_recompute(
         _dtype_code(x), _ptr(g_in), _ptr(g_next), _ptr(x), _ptr(y), _ptr(_f32(phi, "phi")),
         _ptr(_f32(b, "b")), _ptr(_f32(alpha, "alpha")), T, n, D, iters, eps, _ptr(dx), _ptr(dy),
@@ -210,12 +218,13 @@ def mhc_post_pre(x, y, H_post_l, H_res_l, phi, b, alpha, iters: int = 20,
     if y.dtype != x.dtype:
         raise TypeError("x and y must share a dtype")
     f32 = dict(dtype=torch.float32, device=x.device)
-    out = PostPreOut(torch.empty_like(x), torch.empty((T, D), dtype=x.dtype, device=x.device),
-                     torch.empty((T, n), **f32), torch.empty((T, n), **f32),
-                     torch.empty((T, n, n), **f32), torch.empty((T, G), **f32),
-                     torch.empty((T,), **f32))
+    out = PostPreOut(_empty(x.shape, x.dtype, x.device),
+                     _empty((T, D), dtype=x.dtype, device=x.device),
+                     _empty((T, n), **f32), _empty((T, n), **f32),
+                     _empty((T, n, n), **f32), _empty((T, G), **f32),
+                     _empty((T,), **f32))
     nws = int(lib().mhc_post_pre_workspace_bytes(_dtype_code(x), T, n, D))
-    ws = torch.empty((max(nws, 1),), dtype=torch.uint8, device=x.device)
+    ws = _empty((max(nws, 1),), dtype=torch.uint8, device=x.device)
     st = lib().mhc_post_pre(_dtype_code(x), _ptr(x), _ptr(y), _ptr(_f32(H_post_l, "H_post_l")),
                             _ptr(_f32(H_res_l, "H_res_l")), _ptr(_f32(phi, "phi")),
                             _ptr(_f32(b, "b")), _ptr(_f32(alpha, "alpha")), T, n, D, iters, eps,
@@ -230,7 +239,7 @@ def mhc_post_norm(x, y, H_post, H_res, flags: int, eps: float = 1e-6):
     if y.dtype != x.dtype:
         raise TypeError("x and y must share a dtype")
     f32 = dict(dtype=torch.float32, device=x.device)
-    out = PostNormOut(torch.empty_like(x), torch.empty((T,), **f32), torch.empty((T,), **f32))
+    out = PostNormOut(_empty(x.shape, x.dtype, x.device), _empty((T,), **f32), _empty((T,), **f32))
     st = lib().mhc_post_norm(_dtype_code(x), _ptr(x), _ptr(y), _ptr(_f32(H_post, "H_post")),
                              _ptr(_f32(H_res, "H_res")), flags, eps, T, n, D, *[_ptr(o) for o in out],
                              _stream(x.device))
@@ -243,8 +252,8 @@ def mhc_post_norm_bwd(g_next, x, y, H_post, H_res, flags: int, inv_rms_y, inv_rm
     """Gradients of <g_next, x_next> for mhc_post_norm: (dx, dy, dH_post, dH_res)."""
     T, n, D = x.shape
     f32 = dict(dtype=torch.float32, device=x.device)
-    out = PostBwdOut(torch.empty_like(x), torch.empty_like(y), torch.empty((T, n), **f32),
-                     torch.empty((T, n, n), **f32))
+    out = PostBwdOut(_empty(x.shape, x.dtype, x.device), _empty(y.shape, y.dtype, y.device),
+                     _empty((T, n), **f32), _empty((T, n, n), **f32))
     st = lib().mhc_post_norm_bwd(_dtype_code(x), _ptr(g_next), _ptr(x), _ptr(y),
                                  _ptr(_f32(H_post, "H_post")), _ptr(_f32(H_res, "H_res")), flags, eps,
                                  _ptr(_f32(inv_rms_y, "inv_rms_y")), _ptr(_f32(inv_rms_out, "inv_rms_out")),
@@ -258,7 +267,7 @@ def mhc_post(x, y, H_post, H_res):
     T, n, D = x.shape
     if y.dtype != x.dtype:
         raise TypeError("x and y must share a dtype")
-    x_next = torch.empty_like(x)
+    x_next = _empty(x.shape, x.dtype, x.device)
     st = lib().mhc_post(_dtype_code(x), _ptr(x), _ptr(y), _ptr(_f32(H_post, "H_post")),
                         _ptr(_f32(H_res, "H_res")), T, n, D, _ptr(x_next),
                         _stream(x.device))
@@ -272,8 +281,8 @@ def mhc_post_bwd(g_next, x, y, H_post, H_res):
     if not (g_next.dtype == x.dtype == y.dtype):
         raise TypeError("g_next, x and y must share a dtype")
     f32 = dict(dtype=torch.float32, device=x.device)
-    out = PostBwdOut(torch.empty_like(x), torch.empty_like(y),
-                     torch.empty((T, n), **f32), torch.empty((T, n, n), **f32))
+    out = PostBwdOut(_empty(x.shape, x.dtype, x.device), _empty(y.shape, y.dtype, y.device),
+                     _empty((T, n), **f32), _empty((T, n, n), **f32))
     st = lib().mhc_post_bwd(_dtype_code(x), _ptr(g_next), _ptr(x), _ptr(y),
                             _ptr(_f32(H_post, "H_post")), _ptr(_f32(H_res, "H_res")),
                             T, n, D, *[_ptr(o) for o in out], _stream(x.device))
@@ -301,11 +310,11 @@ def mhc_pre_bwd(g_in, dH_post, dH_res, x, phi, b, alpha, proj, inv_rms, dx,
         raise TypeError("g_in, x and dx must share a dtype")
     need = pre_bwd_workspace_bytes(x.dtype, T, n, D)
     if workspace is None:
-        workspace = torch.empty((max(need, 16),), dtype=torch.uint8, device=x.device)
+        workspace = _empty((max(need, 16),), dtype=torch.uint8, device=x.device)
     f32 = dict(dtype=torch.float32, device=x.device)
-    dphi = torch.empty((n * D, G), **f32)
-    db = torch.empty((G,), **f32)
-    dalpha = torch.empty((3,), **f32)
+    dphi = _empty((n * D, G), **f32)
+    db = _empty((G,), **f32)
+    dalpha = _empty((3,), **f32)
     st = lib().mhc_pre_bwd(_dtype_code(x), _ptr(g_in), _ptr(_f32(dH_post, "dH_post")),
                            _ptr(_f32(dH_res, "dH_res")), _ptr(x), _ptr(_f32(phi, "phi")),
                            _ptr(_f32(b, "b")), _ptr(_f32(alpha, "alpha")),
@@ -328,9 +337,9 @@ def mhc_pre_bwd_noalloc(g_in, dH_post, dH_res, x, phi, b, alpha, proj, inv_rms,
     if not (g_in.dtype == x.dtype == dx.dtype):
         raise TypeError("g_in, x and dx must share a dtype")
     f32 = dict(dtype=torch.float32, device=x.device)
-    dphi = torch.empty((n * D, G), **f32)
-    db = torch.empty((G,), **f32)
-    dalpha = torch.empty((3,), **f32)
+    dphi = _empty((n * D, G), **f32)
+    db = _empty((G,), **f32)
+    dalpha = _empty((3,), **f32)
     st = lib().mhc_pre_bwd_noalloc(
         _dtype_code(x), _ptr(g_in), _ptr(_f32(dH_post, "dH_post")), _ptr(_f32(dH_res, "dH_res")),
         _ptr(x), _ptr(_f32(phi, "phi")), _ptr(_f32(b, "b")), _ptr(_f32(alpha, "alpha")),

@@ -70,6 +70,8 @@ cudaError_t launch_pre_tc(const void* x, const float* phi, const float* b, const
                           cudaStream_t s);
 bool pre_tc_supports(int64_t T, int64_t D);
 cudaError_t read_and_clear_device_error(unsigned* word, cudaStream_t s);
+cudaError_t set_force_timeout_pre(unsigned on);   // pre_tc.cu
+cudaError_t set_force_timeout_bwd(unsigned on);   // pre_bwd_fused.cu
 // Defined in post_pre_tc.cu: layer l's residual update fused with layer
 // l + 1's pre forward (bf16).
 bool post_pre_tc_supports(int64_t T, int64_t D);
@@ -100,6 +102,12 @@ mhc_status mhc_get_last_device_error(cudaStream_t stream) {
     unsigned word = 0;
     if (mhc::read_and_clear_device_error(&word, stream) != cudaSuccess) return MHC_ERR_CUDA;
     return word == 0 ? MHC_OK : MHC_ERR_TIMEOUT;
+}
+
+mhc_status mhc_test_force_timeout(int on) {
+    const unsigned v = on ? 1u : 0u;
+    if (mhc::set_force_timeout_pre(v) != cudaSuccess) return MHC_ERR_CUDA;
+    return from_cuda(mhc::set_force_timeout_bwd(v));
 }
 
 mhc_status mhc_pre(mhc_dtype dt, const void* x, const float* phi, const float* b,

@@ -65,6 +65,13 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 // This file's device error word (latched by bounded waits that ran out).
 __device__ unsigned g_bwd_fused_error;
+// Test hook (mhc_test_force_timeout): nonzero makes pre_bwd_fused_kernel run
+// one bounded wait that nothing completes, then return.
+__device__ unsigned g_force_timeout_bwd;
+
+cudaError_t set_force_timeout_bwd(unsigned on) {
+    return cudaMemcpyToSymbol(g_force_timeout_bwd, &on, sizeof(unsigned));
+}
 
 cudaError_t read_and_clear_bwd_fused_error(unsigned* word) {
     cudaError_t e = cudaMemcpyFromSymbol(word, g_bwd_fused_error, sizeof(unsigned));
@@ -214,6 +221,16 @@ pre_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Layout::MISC + 16);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (g_force_timeout_bwd != 0u) {
+        // test hook: one bounded wait that runs out, before anything async
+        // starts; the kernel still waits for the per-token kernel it may
+        // have started beside (programmatic dependent launch) before leaving
+        if (tid == 0 && ptx::forced_wait_runs_out(ptx::smem_u32(smem), 100000ull))
+            atomicOr(&g_bwd_fused_error, 1u);
+        __syncthreads();
+        ptx::griddep_wait();
+        return;
+    }
     constexpr unsigned FULL = 0xffffffffu;
     const uint32_t C = ptx::cluster_nctarank();
     const uint32_t rank = ptx::cluster_ctarank();

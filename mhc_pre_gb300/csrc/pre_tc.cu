@@ -56,6 +56,13 @@ namespace mhc {
 // Latched by kernels whose bounded waits ran out; read and cleared by
 // mhc_get_last_device_error().
 __device__ unsigned g_device_error;
+// Test hook (mhc_test_force_timeout): nonzero makes pre_tc_kernel run one
+// bounded wait that nothing completes, then return.
+__device__ unsigned g_force_timeout_pre;
+
+cudaError_t set_force_timeout_pre(unsigned on) {
+    return cudaMemcpyToSymbol(g_force_timeout_pre, &on, sizeof(unsigned));
+}
 
 cudaError_t read_and_clear_bwd_tc_error(unsigned* word);      // pre_bwd_tc.cu
 cudaError_t read_and_clear_bwd_fused_error(unsigned* word);   // pre_bwd_fused.cu
@@ -202,6 +209,14 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
     const float* recv = reinterpret_cast<const float*>(smem + L.recv);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (g_force_timeout_pre != 0u) {
+        // test hook: one bounded wait that runs out, before anything async
+        // starts; every CTA of the launch takes this path and none touches a
+        // peer, so leaving here is safe
+        if (tid == 0 && ptx::forced_wait_runs_out(ptx::smem_u32(smem), 100000ull)) atomicOr(&g_device_error, 1u);
+        __syncthreads();
+        return;
+    }
     const uint32_t c = ptx::cluster_ctarank();
     const int cid = static_cast<int>(ptx::cluster_id_x());
     const int ncl = static_cast<int>(ptx::nclusters_x());

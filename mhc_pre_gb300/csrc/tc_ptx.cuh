@@ -84,6 +84,20 @@ __device__ __forceinline__ uint64_t globaltimer() {
     return t;
 }
 
+// Test hook of the bounded waits: when `armed`, thread 0 of the CTA waits on
+// a fresh mbarrier that nothing ever arrives on, gives up after `limit_ns`
+// and returns true (the caller latches its device error word and leaves
+// before any copy, TMEM allocation or cluster exchange has started).
+__device__ __forceinline__ bool forced_wait_runs_out(uint32_t bar, uint64_t limit_ns) {
+    mbar_init(bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, 0)) {
+        if (globaltimer() - t0 > limit_ns) return true;
+    }
+    return false;
+}
+
 // ----------------------------------------------------------------- cluster
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
