@@ -368,7 +368,7 @@ def main():
         if e: e[0].record(stream)
         f = B.mhc_pre(a["x"], a["phi"], a["b"], a["alpha"], w.iters, w.eps)
         if e: e[1].record(stream)
-        B.mhc_post(a["x"], a["y"], f.H_post, f.H_res)
+        xn = B.mhc_post(a["x"], a["y"], f.H_post, f.H_res)
         if e: e[2].record(stream)
         pb = B.mhc_post_bwd(a["g_next"], a["x"], a["y"], f.H_post, f.H_res)
         if e: e[3].record(stream)
@@ -377,7 +377,8 @@ def main():
         if e: e[4].record(stream)
         if world > 1:
             allreduce_param_grads(qb.dphi, qb.db, qb.dalpha)
-        return qb
+        return {"x_in": f.x_in, "x_next": xn, "dx": qb.dx, "dy": pb.dy,
+                "dphi": qb.dphi, "db": qb.db, "dalpha": qb.dalpha}
 
     for _ in range(args.warmup):
         step()
@@ -428,11 +429,13 @@ def main():
         e2e = run_e2e(args, w, inp, step, stream, dev, world)
 
     # ---- side measurement: the cross-layer step (rank 0, N = 1) --------------
-    cross = post_norm = recompute = None
+    cross = post_norm = recompute = decode = sweep = None
     if rank == 0 and world == 1 and not args.no_cross_layer:
         cross = run_cross_layer(w, inp, dev)
         post_norm = run_post_norm(w, inp, dev)
         recompute = run_recompute(w, inp, dev)
+        decode = run_decode(w, dev)
+        sweep = run_sweep(w, inp, dev)
 
     # ---- float64 oracle on the host cores (rank 0, N = 1) --------------------
     cpu = None
@@ -458,6 +461,14 @@ def main():
         "step_hbm": {"GBps": step_bytes / (elapsed_ms / args.steps) / 1e6,
                      "frac_of_" + peak_kind: step_bytes / (elapsed_ms / args.steps) / 1e6 / peak,
                      "frac_of_8TBps_nominal": step_bytes / (elapsed_ms / args.steps) / 1e6 / NOMINAL_HBM_GBS},
+        "roofline_forward": {"bound": "hbm", "kernel": "mhc_pre",
+                             "achieved": nbytes["mhc_pre"] / per_op_ms["mhc_pre"] / 1e6,
+                             "peak": NOMINAL_HBM_GBS, "peak_kind": "nominal 8 TB/s",
+                             "unit": "GB/s",
+                             "frac": nbytes["mhc_pre"] / per_op_ms["mhc_pre"] / 1e6 / NOMINAL_HBM_GBS,
+                             "frac_of_" + peak_kind: nbytes["mhc_pre"] / per_op_ms["mhc_pre"] / 1e6 / peak,
+                             "target_frac": 0.70,
+                             "target_met": nbytes["mhc_pre"] / per_op_ms["mhc_pre"] / 1e6 >= 0.70 * NOMINAL_HBM_GBS},
         "kernels": kernels,
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -466,6 +477,9 @@ def main():
         "cross_layer": cross,
         "post_norm": post_norm,
         "recompute": recompute,
+        "decode": decode,
+        "sinkhorn_sweep": sweep,
+        "memory": memory_accounting(w),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -513,24 +527,32 @@ def ncu_traffic(op, w):
 
 
 def run_e2e(args, w, inp, step, stream, dev, world):
-    """The step through the public API with the host in the loop: every
-    step's inputs are copied from pinned host memory and its parameter
-    gradients copied back, all inside the timed region.  The inputs of step
+    """The step through the public API with the host in the loop, as a round
+    trip: every step's inputs are copied from pinned host memory, and every
+    result (x_in, x_next, dx, dy and the parameter gradients) copied back to
+    pinned host memory, all inside the timed region.  The inputs of step
     i + 1 are copied on a second stream into a second set of device buffers
-    while step i computes (the copies, bound by the host link, dominate)."""
+    while step i computes; the results of step i are copied back on a third
+    stream while step i + 1 computes (the copies, bound by the host link,
+    dominate)."""
     import torch
     host = {k: v.to("cpu").pin_memory() for k, v in inp.items()}
     keys = ("x", "y", "g_in", "g_next", "phi", "b", "alpha")
     h2d = sum(host[k].numel() * host[k].element_size() for k in keys)
-    G = w.G
-    out_h = {"dphi": torch.empty((w.K, G), pin_memory=True),
-             "db": torch.empty((G,), pin_memory=True),
+    act = inp["x"].dtype
+    out_h = {"x_in": torch.empty((w.T, w.D), dtype=act, pin_memory=True),
+             "x_next": torch.empty((w.T, w.n, w.D), dtype=act, pin_memory=True),
+             "dx": torch.empty((w.T, w.n, w.D), dtype=act, pin_memory=True),
+             "dy": torch.empty((w.T, w.D), dtype=act, pin_memory=True),
+             "dphi": torch.empty((w.K, w.G), pin_memory=True),
+             "db": torch.empty((w.G,), pin_memory=True),
              "dalpha": torch.empty((3,), pin_memory=True)}
     d2h = sum(v.numel() * v.element_size() for v in out_h.values())
     bufs = [{k: inp[k] for k in keys}, {k: torch.empty_like(inp[k]) for k in keys}]
-    copy_stream = torch.cuda.Stream(dev)
+    copy_stream, back_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     copied = [torch.cuda.Event(), torch.cuda.Event()]
     consumed = [torch.cuda.Event(), torch.cuda.Event()]
+    computed = torch.cuda.Event()
 
     def copy_in(bi):
         with torch.cuda.stream(copy_stream):
@@ -538,6 +560,14 @@ def run_e2e(args, w, inp, step, stream, dev, world):
             for k in keys:
                 bufs[bi][k].copy_(host[k], non_blocking=True)
             copied[bi].record(copy_stream)
+
+    def copy_out(res):
+        computed.record(stream)
+        back_stream.wait_event(computed)
+        with torch.cuda.stream(back_stream):
+            for k, t in res.items():
+                out_h[k].copy_(t, non_blocking=True)
+                t.record_stream(back_stream)            # not reused before the copy is done
 
     def run(n):
         for ev in consumed:
@@ -548,11 +578,10 @@ def run_e2e(args, w, inp, step, stream, dev, world):
             stream.wait_event(copied[bi])
             if i + 1 < n:
                 copy_in(bi ^ 1)
-            qb = step(src=bufs[bi])
+            res = step(src=bufs[bi])
             consumed[bi].record(stream)
-            out_h["dphi"].copy_(qb.dphi, non_blocking=True)
-            out_h["db"].copy_(qb.db, non_blocking=True)
-            out_h["dalpha"].copy_(qb.dalpha, non_blocking=True)
+            copy_out(res)
+        stream.wait_stream(back_stream)                 # the last results are on the host
 
     steps = args.steps
     run(min(3, args.warmup))
@@ -572,7 +601,113 @@ def run_e2e(args, w, inp, step, stream, dev, world):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": ms / steps,
             "path": "pinned host -> device copies (next step's on a second stream, overlapping this "
-                    "step's compute), the four C-ABI calls, parameter gradients -> pinned host"}
+                    "step's compute), the four C-ABI calls, every result (x_in, x_next, dx, dy, dphi, "
+                    "db, dalpha) -> pinned host on a third stream (overlapping the next step)"}
+
+
+def graph_latency_us(fn, dev, calls=20, reps=7):
+    """Device time of one call of `fn`, from a CUDA graph of `calls`
+    back-to-back calls replayed `reps` times (median), so host launch overhead
+    does not count."""
+    import torch
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(calls):
+            fn()
+    ts = []
+    with torch.cuda.stream(s):   # replay() launches on the current stream
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            g.replay()
+            b.record(s)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3 / calls)
+    return statistics.median(ts)
+
+
+def run_decode(w, dev):
+    """Decode-sized batches (T = 1, 8, 64 at the workload's width): latency of
+    mhc_pre, of the inference critical path (mhc_pre_critical: x_in, H_pre,
+    saved state) and of its side (mhc_post_res_gates: H_post, H_res with
+    Sinkhorn, which a second stream overlaps with the sublayer)."""
+    from mhc_pre_gb300 import binding as B
+    from mhc_pre_gb300 import workloads as W
+    out = {}
+    for T in (1, 8, 64):
+        wd = w.with_(T=T, backward=False)
+        inp = W.make_inputs(wd, device=dev)
+        x, phi, b, alpha = inp["x"], inp["phi"], inp["b"], inp["alpha"]
+        c = B.mhc_pre_critical(x, phi, b, alpha, wd.eps)
+        out[str(T)] = {
+            "mhc_pre_us": graph_latency_us(lambda: B.mhc_pre(x, phi, b, alpha, wd.iters, wd.eps), dev),
+            "critical_path_us": graph_latency_us(lambda: B.mhc_pre_critical(x, phi, b, alpha, wd.eps), dev),
+            "side_gates_us": graph_latency_us(lambda: B.mhc_post_res_gates(c.proj, b, alpha, wd.iters), dev),
+        }
+    assert B.get_last_device_error() == B.MHC_OK
+    return {"op": "mhc_pre / mhc_pre_critical + mhc_post_res_gates (side stream)",
+            "timing": "CUDA graph of 20 calls, median of 7 replays, inputs L2-warm", "T": out}
+
+
+def run_sweep(w, inp, dev, reps=10):
+    """The Sinkhorn round count of the large-batch workload swept over
+    {5, 20, 50}: time of each op that runs Sinkhorn (mhc_pre forward, the
+    mhc_pre_bwd recompute with its reverse pass)."""
+    import torch
+    from mhc_pre_gb300 import binding as B
+    stream = torch.cuda.current_stream(dev)
+    x, y, phi, b, alpha = (inp[k] for k in ("x", "y", "phi", "b", "alpha"))
+    ws = torch.empty((B.pre_bwd_workspace_bytes(x.dtype, w.T, w.n, w.D),), dtype=torch.uint8, device=dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(reps):
+            fn()
+        e.record(stream)
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) / reps
+
+    out = {}
+    for iters in (5, 20, 50):
+        f = B.mhc_pre(x, phi, b, alpha, iters, w.eps)
+        pb = B.mhc_post_bwd(inp["g_next"], x, y, f.H_post, f.H_res)
+        dx0 = pb.dx.clone()
+        out[str(iters)] = {
+            "mhc_pre_ms": timed(lambda: B.mhc_pre(x, phi, b, alpha, iters, w.eps)),
+            "mhc_pre_bwd_ms": timed(lambda: B.mhc_pre_bwd(inp["g_in"], pb.dH_post, pb.dH_res, x, phi, b, alpha,
+                                                          f.proj, f.inv_rms, dx0, iters, workspace=ws)),
+        }
+    assert B.get_last_device_error() == B.MHC_OK
+    return {"op": "Sinkhorn rounds swept (large-batch workload)", "iters": out}
+
+
+def memory_accounting(w):
+    """What the backward of one mHC layer keeps per token beyond its inputs,
+    set beside the Ascend mHC operator article's count for an unfused
+    composition: 2 (7N - 3) B S D bytes more per layer (bf16 values).  Both
+    modes keep x (the hc_pre input) and y (the sublayer output), as any
+    residual layer does; the saved-state mode adds proj and inv_rms, 100 B per
+    token for each mHC op, and the recompute mode (mhc_layer_bwd_recompute)
+    adds nothing.  A layer has two mHC ops (attention and MLP/MoE); across
+    layers, mhc_post_pre restores layer l + 1's x from layer l's (x, y)."""
+    N, D = w.n, w.D
+    pages = 2 * (7 * N - 3) * D
+    saved = 2 * 4 * (w.G + 1)
+    B_, S_ = 1, 4096
+    return {"per_token_bytes_per_layer": {"pages_unfused_extra": pages, "saved_state": saved, "recompute": 0},
+            "per_layer_bytes_B1_S4096": {"pages_unfused_extra": pages * B_ * S_,
+                                         "saved_state": saved * B_ * S_, "recompute": 0},
+            "saved_state_fraction_of_pages": saved / pages,
+            "formula": "2*(7N-3)*B*S*D (pages), N=%d D=%d" % (N, D)}
 
 
 if __name__ == "__main__":

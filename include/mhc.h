@@ -208,6 +208,7 @@ mhc_status mhc_post_bwd(mhc_dtype dt, const void* g_next, const void* x,
 mhc_status mhc_test_force_timeout(int on);
 
 /* Number of kernels the entry point `op` ("mhc_pre", "mhc_pre_gates",
+ * "mhc_pre_critical", "mhc_post_res_gates",
  * "mhc_post", "mhc_post_norm", "mhc_post_norm_bwd", "mhc_post_pre",
  * "mhc_post_bwd", "mhc_pre_bwd" or "mhc_layer_bwd_recompute") launches for these sizes; -1 for an
  * unknown op or sizes the entry point would reject.  Useful when sizing CUDA
@@ -292,6 +293,41 @@ mhc_status mhc_pre_bwd_noalloc(mhc_dtype dt, const void* g_in, const float* dH_p
                                const float* inv_rms, int64_t T, int n, int64_t D, int iters,
                                void* dx, float* dphi, float* db, float* dalpha,
                                cudaStream_t stream);
+
+/*
+ * The inference critical-path split.  The openPangu 2.0 notes (section 11.3,
+ * the inference system) put the previous layer's merge, the RMSNorm and H^pre
+ * on the critical path that feeds the sublayer, and move H^post and H^res
+ * (with Sinkhorn) to a low-priority side stream that overlaps the sublayer.
+ * The two calls below are that split: mhc_pre_critical writes what the
+ * sublayer needs (x_in) and the saved state; mhc_post_res_gates computes
+ * H^post and H^res from the saved projection and may run on another stream,
+ * ordered after mhc_pre_critical by an event.  Together they write the same
+ * values as mhc_pre, bit for bit.
+ */
+
+/*
+ * mhc_pre_critical -- mhc_pre without H_post, H_res and Sinkhorn: x_in,
+ * H_pre, proj and inv_rms exactly as mhc_pre writes them (same kernels and
+ * arithmetic).  Arguments, layouts, ownership and errors as mhc_pre; there is
+ * no iters (no Sinkhorn runs).
+ */
+mhc_status mhc_pre_critical(mhc_dtype dt, const void* x, const float* phi, const float* b,
+                            const float* alpha, int64_t T, int n, int64_t D, float eps, void* x_in,
+                            float* H_pre, float* proj, float* inv_rms, cudaStream_t stream);
+
+/*
+ * mhc_post_res_gates -- H_post = 2 sigmoid(logits[n:2n]) and H_res =
+ * Sinkhorn(exp(reshape(logits[2n:], n, n))), `iters` rounds, from the
+ * projection proj [T, 2n+n^2] (float32, as mhc_pre / mhc_pre_critical wrote
+ * it), with logits = alpha_group * proj + b as in mhc_pre.  Writes H_post
+ * [T, n] and H_res [T, n, n] (float32), bit for bit the values mhc_pre
+ * writes.  proj must be complete on `stream` (an event if it was written on
+ * another one).  n must be 4; iters in [1, MHC_MAX_ITERS]; every pointer
+ * 16-byte aligned; T = 0 is a no-op.
+ */
+mhc_status mhc_post_res_gates(const float* proj, const float* b, const float* alpha, int64_t T, int n,
+                              int iters, float* H_post, float* H_res, cudaStream_t stream);
 
 /*
  * Recompute-oriented backward.  The Ascend mHC Triton operator article

@@ -30,7 +30,8 @@ EXPORTS = ("mhc_status_string", "mhc_version", "mhc_get_last_device_error",
            "mhc_post_bwd", "mhc_kernel_launches",
            "mhc_pre_bwd_workspace_bytes", "mhc_pre_bwd", "mhc_pre_bwd_noalloc",
            "mhc_pre_gates", "mhc_layer_bwd_recompute_workspace_bytes",
-           "mhc_layer_bwd_recompute", "mhc_test_force_timeout")
+           "mhc_layer_bwd_recompute", "mhc_test_force_timeout", "mhc_pre_critical",
+           "mhc_post_res_gates")
 
 PreOut = namedtuple("PreOut", "x_in H_pre H_post H_res proj inv_rms")
 PostPreOut = namedtuple("PostPreOut", "x_next x_in H_pre H_post H_res proj inv_rms")
@@ -39,6 +40,8 @@ SANDWICH_NORM, BLOCK_NORM = 1, 2
 PostBwdOut = namedtuple("PostBwdOut", "dx dy dH_post dH_res")
 PreBwdOut = namedtuple("PreBwdOut", "dx dphi db dalpha")
 PreGatesOut = namedtuple("PreGatesOut", "H_pre H_post H_res proj inv_rms")
+PreCriticalOut = namedtuple("PreCriticalOut", "x_in H_pre proj inv_rms")
+PostResGatesOut = namedtuple("PostResGatesOut", "H_post H_res")
 LayerBwdOut = namedtuple("LayerBwdOut", "dx dy dphi db dalpha")
 
 _P, _I64, _I, _F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
@@ -67,6 +70,8 @@ _SIGS = {
                        _P, _P, _P, _P, _P, _P], _I),
     "mhc_layer_bwd_recompute_workspace_bytes": ([_I, _I64, _I, _I64], ctypes.c_size_t),
     "mhc_test_force_timeout": ([_I], _I),
+    "mhc_pre_critical": ([_I, _P, _P, _P, _P, _I64, _I, _I64, _F, _P, _P, _P, _P, _P], _I),
+    "mhc_post_res_gates": ([_P, _P, _P, _I64, _I, _I, _P, _P, _P], _I),
     "mhc_layer_bwd_recompute": ([_I, _P, _P, _P, _P, _P, _P, _P, _I64, _I, _I64, _I, _F,
                                  _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P], _I),
 }
@@ -182,6 +187,35 @@ def mhc_pre_gates(x, phi, b, alpha, iters: int = 20, eps: float = 1e-6):
 def layer_bwd_recompute_workspace_bytes(dtype, T: int, n: int, D: int) -> int:
     code = MHC_BF16 if dtype == torch.bfloat16 else MHC_F32
     return int(lib().mhc_layer_bwd_recompute_workspace_bytes(code, T, n, D))
+
+
+def mhc_pre_critical(x, phi, b, alpha, eps: float = 1e-6, stream=None):
+    """The inference critical path of mhc_pre: x_in, H_pre, proj, inv_rms (no
+    Sinkhorn).  ``stream``: a torch.cuda.Stream (default: the current one)."""
+    T, n, D = x.shape
+    G = 2 * n + n * n
+    f32 = dict(dtype=torch.float32, device=x.device)
+    out = PreCriticalOut(_empty((T, D), dtype=x.dtype, device=x.device), _empty((T, n), **f32),
+                         _empty((T, G), **f32), _empty((T,), **f32))
+    s = stream.cuda_stream if stream is not None else _stream(x.device)
+    st = lib().mhc_pre_critical(_dtype_code(x), _ptr(x), _ptr(_f32(phi, "phi")), _ptr(_f32(b, "b")),
+                                _ptr(_f32(alpha, "alpha")), T, n, D, eps, *[_ptr(o) for o in out], s)
+    _check(st, "mhc_pre_critical")
+    return out
+
+
+def mhc_post_res_gates(proj, b, alpha, iters: int = 20, stream=None):
+    """H_post and H_res from a saved projection (the side of the critical-path
+    split).  ``stream``: a torch.cuda.Stream (default: the current one)."""
+    T, G = proj.shape
+    n = 4
+    f32 = dict(dtype=torch.float32, device=proj.device)
+    out = PostResGatesOut(_empty((T, n), **f32), _empty((T, n, n), **f32))
+    s = stream.cuda_stream if stream is not None else _stream(proj.device)
+    st = lib().mhc_post_res_gates(_ptr(_f32(proj, "proj")), _ptr(_f32(b, "b")), _ptr(_f32(alpha, "alpha")),
+                                  T, n, iters, *[_ptr(o) for o in out], s)
+    _check(st, "mhc_post_res_gates")
+    return out
 
 
 def mhc_layer_bwd_recompute(g_in, g_next, x, y, phi, b, alpha, iters: int = 20,

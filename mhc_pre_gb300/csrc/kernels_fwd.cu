@@ -151,18 +151,26 @@ pre_proj_gates_kernel(const TA* __restrict__ x, const float* __restrict__ phi,
             float proj[NG];
 #pragma unroll
             for (int g = 0; g < NG; ++g) proj[g] = z[g] * inv;
-            float hp[4], hq[4], hr[16];
-            token_gates(proj, alpha, b, iters, hp, hq, hr);
             float4* po = reinterpret_cast<float4*>(proj_out + t * NG);
 #pragma unroll
             for (int v = 0; v < NG / 4; ++v)
                 po[v] = make_float4(proj[4 * v], proj[4 * v + 1], proj[4 * v + 2], proj[4 * v + 3]);
             inv_rms_out[t] = inv;
-            reinterpret_cast<float4*>(H_pre)[t] = make_float4(hp[0], hp[1], hp[2], hp[3]);
-            reinterpret_cast<float4*>(H_post)[t] = make_float4(hq[0], hq[1], hq[2], hq[3]);
-            float4* hro = reinterpret_cast<float4*>(H_res + t * 16);
+            if (H_res == nullptr) {
+                // the critical path: H_pre only, no Sinkhorn
+                float hp[4];
+                token_pre_gates(proj, alpha, b, hp);
+                reinterpret_cast<float4*>(H_pre)[t] = make_float4(hp[0], hp[1], hp[2], hp[3]);
+            } else {
+                float hp[4], hq[4], hr[16];
+                token_gates(proj, alpha, b, iters, hp, hq, hr);
+                reinterpret_cast<float4*>(H_pre)[t] = make_float4(hp[0], hp[1], hp[2], hp[3]);
+                reinterpret_cast<float4*>(H_post)[t] = make_float4(hq[0], hq[1], hq[2], hq[3]);
+                float4* hro = reinterpret_cast<float4*>(H_res + t * 16);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) hro[v] = make_float4(hr[4 * v], hr[4 * v + 1], hr[4 * v + 2], hr[4 * v + 3]);
+                for (int v = 0; v < 4; ++v)
+                    hro[v] = make_float4(hr[4 * v], hr[4 * v + 1], hr[4 * v + 2], hr[4 * v + 3]);
+            }
         }
     }
 }
@@ -261,6 +269,39 @@ cudaError_t launch_pre_cc(bool bf16, const void* x, const float* phi, const floa
             pre_mix_kernel<float><<<g2, 256, 0, s>>>(static_cast<const float*>(x), H_pre, T, D,
                                                      static_cast<float*>(x_in));
     }
+    return cudaGetLastError();
+}
+
+// H_post and H_res of each token from its saved projection (thread per
+// token): the side of the inference critical-path split.
+__global__ void __launch_bounds__(128)
+post_res_gates_kernel(const float* __restrict__ proj, const float* __restrict__ b,
+                      const float* __restrict__ alpha, int64_t T, int iters, float* __restrict__ H_post,
+                      float* __restrict__ H_res) {
+    __shared__ float par[3 + NG];
+    if (threadIdx.x < 3) par[threadIdx.x] = alpha[threadIdx.x];
+    if (threadIdx.x < NG) par[3 + threadIdx.x] = b[threadIdx.x];
+    __syncthreads();
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (t >= T) return;
+    float pj[NG];
+#pragma unroll
+    for (int v = 0; v < NG / 4; ++v) {
+        const float4 a = reinterpret_cast<const float4*>(proj + t * NG)[v];
+        pj[4 * v] = a.x; pj[4 * v + 1] = a.y; pj[4 * v + 2] = a.z; pj[4 * v + 3] = a.w;
+    }
+    float hq[4], hr[16];
+    token_post_res_gates(pj, par, par + 3, iters, hq, hr);
+    reinterpret_cast<float4*>(H_post)[t] = make_float4(hq[0], hq[1], hq[2], hq[3]);
+    float4* hro = reinterpret_cast<float4*>(H_res + t * 16);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) hro[v] = make_float4(hr[4 * v], hr[4 * v + 1], hr[4 * v + 2], hr[4 * v + 3]);
+}
+
+cudaError_t launch_post_res_gates(const float* proj, const float* b, const float* alpha, int64_t T, int iters,
+                                  float* H_post, float* H_res, cudaStream_t s) {
+    post_res_gates_kernel<<<static_cast<unsigned>((T + 127) / 128), 128, 0, s>>>(proj, b, alpha, T, iters,
+                                                                               H_post, H_res);
     return cudaGetLastError();
 }
 

@@ -41,6 +41,11 @@ cudaError_t launch_pre_cc(bool bf16, const void* x, const float* phi, const floa
                           void* x_in, float* H_pre, float* H_post, float* H_res,
                           float* proj, float* inv_rms, cudaStream_t s);
 
+// H_post and H_res from a saved projection (the side of the inference
+// critical-path split).
+cudaError_t launch_post_res_gates(const float* proj, const float* b, const float* alpha, int64_t T, int iters,
+                                  float* H_post, float* H_res, cudaStream_t s);
+
 cudaError_t launch_post(bool bf16, const void* x, const void* y, const float* H_post,
                         const float* H_res, int64_t T, int64_t D, void* x_next,
                         cudaStream_t s);

@@ -145,6 +145,39 @@ mhc_status mhc_pre_gates(mhc_dtype dt, const void* x, const float* phi, const fl
                                         H_pre, H_post, H_res, proj, inv_rms, stream));
 }
 
+mhc_status mhc_pre_critical(mhc_dtype dt, const void* x, const float* phi, const float* b,
+                            const float* alpha, int64_t T, int n, int64_t D, float eps, void* x_in,
+                            float* H_pre, float* proj, float* inv_rms, cudaStream_t stream) {
+    const void* ptrs[] = {x, phi, b, alpha, x_in, H_pre, proj, inv_rms};
+    mhc_status st = check_common(dt, T, n, D, ptrs, 8);
+    if (st != MHC_OK) return st;
+    if (!(eps >= 0.0f) || !isfinite(eps)) return MHC_ERR_INVALID_ARG;
+    if (T == 0) return MHC_OK;
+    // the forward kernels with no H_post / H_res buffers skip Sinkhorn and
+    // those gates (iters is then unused)
+    if (dt == MHC_BF16 && mhc::pre_tc_supports(T, D))
+        return from_cuda(mhc::launch_pre_tc(x, phi, b, alpha, T, D, 1, eps, x_in, H_pre, nullptr, nullptr, proj,
+                                            inv_rms, stream));
+    return from_cuda(mhc::launch_pre_cc(dt == MHC_BF16, x, phi, b, alpha, T, D, 1, eps, x_in, H_pre, nullptr,
+                                        nullptr, proj, inv_rms, stream));
+}
+
+mhc_status mhc_post_res_gates(const float* proj, const float* b, const float* alpha, int64_t T, int n,
+                              int iters, float* H_post, float* H_res, cudaStream_t stream) {
+    if (T < 0) return MHC_ERR_INVALID_ARG;
+    if (n != 4) return MHC_ERR_UNSUPPORTED;
+    if (T > (int64_t(1) << 31)) return MHC_ERR_UNSUPPORTED;
+    mhc_status st = check_iters(iters);
+    if (st != MHC_OK) return st;
+    if (T == 0) return MHC_OK;
+    const void* ptrs[] = {proj, b, alpha, H_post, H_res};
+    for (const void* p : ptrs) {
+        if (p == nullptr) return MHC_ERR_INVALID_ARG;
+        if (!aligned16(p)) return MHC_ERR_MISALIGNED;
+    }
+    return from_cuda(mhc::launch_post_res_gates(proj, b, alpha, T, iters, H_post, H_res, stream));
+}
+
 mhc_status mhc_post(mhc_dtype dt, const void* x, const void* y, const float* H_post,
                     const float* H_res, int64_t T, int n, int64_t D, void* x_next,
                     cudaStream_t stream) {
@@ -243,7 +276,9 @@ int mhc_kernel_launches(const char* op, mhc_dtype dt, int64_t T, int n, int64_t 
         return 1 + (dt == MHC_BF16 && mhc::pre_tc_supports(T, D) ? 1 : 2);
     }
     if (strcmp(op, "mhc_pre_bwd") == 0) return 5;   // both paths: 5 launches
-    if (strcmp(op, "mhc_pre_gates") == 0) return 1;
+    if (strcmp(op, "mhc_pre_gates") == 0) return 1;   // no mix: one kernel on either path
+    if (strcmp(op, "mhc_pre_critical") == 0) return dt == MHC_BF16 && mhc::pre_tc_supports(T, D) ? 1 : 2;
+    if (strcmp(op, "mhc_post_res_gates") == 0) return 1;
     if (strcmp(op, "mhc_layer_bwd_recompute") == 0) return 1 + 1 + 5;
     return -1;
 }

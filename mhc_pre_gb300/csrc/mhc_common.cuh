@@ -194,6 +194,26 @@ static __device__ __noinline__ void sinkhorn_vjp(const float* L, int iters, cons
     for (int e = 0; e < 16; ++e) dL[e] = g[e] * M0[e];
 }
 
+// H_pre alone (the inference critical path): the same expression as in
+// token_gates.
+__device__ __forceinline__ void token_pre_gates(const float (&proj)[NG], const float* alpha,
+                                                const float* b, float (&hpre)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) hpre[i] = sigmoid_f(fmaf(alpha[0], proj[i], b[i]));
+}
+
+// H_post and H_res from the projection (the side of the critical-path
+// split): the same expressions as in token_gates.
+__device__ __forceinline__ void token_post_res_gates(const float (&proj)[NG], const float* alpha,
+                                                     const float* b, int iters, float (&hpost)[4],
+                                                     float (&hres)[16]) {
+    float lg[NG];
+    make_logits(proj, alpha, b, lg);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) hpost[i] = 2.0f * sigmoid_f(lg[NS + i]);
+    sinkhorn_fwd(lg + 2 * NS, iters, hres);
+}
+
 // All gates of one token from its projection.
 __device__ __forceinline__ void token_gates(const float (&proj)[NG], const float* alpha,
                                             const float* b, int iters, float (&hpre)[4],

@@ -506,13 +506,18 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
                     }
                     inv = rec[NG / 4].x;
                 }
-                float hp[4], hq[4], hr[16];
-                token_gates(pj, gate_par, gate_par + 3, p.iters, hp, hq, hr);
+                float hp[4], hq[4] = {0.f, 0.f, 0.f, 0.f}, hr[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) hr[e] = 0.f;
+                const bool side = p.H_res != nullptr;   // null: the critical path, no Sinkhorn
+                if (side) token_gates(pj, gate_par, gate_par + 3, p.iters, hp, hq, hr);
+                else token_pre_gates(pj, gate_par, gate_par + 3, hp);
                 const int64_t t = t0 + static_cast<int>(c) * TPC + tt;
                 if (real && t < p.T) {
 #pragma unroll
                     for (int rep = 0; rep < 2; ++rep) {
                         const int k = l8 + 8 * rep;
+                        if (!side && k >= 8) continue;
                         float4 o = make_float4(hp[0], hp[1], hp[2], hp[3]);
 #pragma unroll
                         for (int v = 0; v < NG / 4; ++v)

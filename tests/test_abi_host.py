@@ -219,3 +219,28 @@ def test_layer_bwd_recompute_workspace_and_validation(L):
     assert call(iters=B.MAX_ITERS + 1) == B.MHC_ERR_UNSUPPORTED
     assert call(T=0, ws_ptr=None, dx=None, dphi=None) == B.MHC_ERR_INVALID_ARG
     assert call(T=0, ws_ptr=None, dx=None, dphi=MIS) == B.MHC_ERR_MISALIGNED
+
+
+def test_critical_path_validation(L):
+    def crit(dt=B.MHC_BF16, x=A, T=8, n=4, D=64, eps=1e-6, outs=None):
+        outs = outs or [A] * 4
+        return L.mhc_pre_critical(dt, x, A, A, A, T, n, D, eps, *outs, None)
+
+    assert crit(n=3) == B.MHC_ERR_UNSUPPORTED
+    assert crit(D=60) == B.MHC_ERR_UNSUPPORTED
+    assert crit(x=None) == B.MHC_ERR_INVALID_ARG
+    assert crit(outs=[A, MIS, A, A]) == B.MHC_ERR_MISALIGNED
+    assert crit(eps=float("nan")) == B.MHC_ERR_INVALID_ARG
+    assert L.mhc_pre_critical(B.MHC_BF16, *([None] * 4), 0, 4, 64, 1e-6, *([None] * 4), None) == B.MHC_OK
+
+    def side(T=8, n=4, iters=20, proj=A, outs=None):
+        outs = outs or [A, A]
+        return L.mhc_post_res_gates(proj, A, A, T, n, iters, *outs, None)
+
+    assert side(n=2) == B.MHC_ERR_UNSUPPORTED
+    assert side(iters=0) == B.MHC_ERR_INVALID_ARG
+    assert side(iters=B.MAX_ITERS + 1) == B.MHC_ERR_UNSUPPORTED
+    assert side(proj=None) == B.MHC_ERR_INVALID_ARG
+    assert side(outs=[A, MIS]) == B.MHC_ERR_MISALIGNED
+    assert side(T=-1) == B.MHC_ERR_INVALID_ARG
+    assert L.mhc_post_res_gates(None, None, None, 0, 4, 20, None, None, None) == B.MHC_OK
