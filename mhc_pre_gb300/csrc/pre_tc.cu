@@ -102,8 +102,10 @@ constexpr int PHI_CHUNK_BYTES = NB * KW * 2;      // 6 KB
 constexpr int MAX_NCH = 20;                       // K-slice <= 1280 columns
 constexpr int NTHREADS = 512;                     // 16 warps
 constexpr int GATE_WARP0 = 2, NGATE = 4;          // TMEM readers, cluster reduction, H_pre
-constexpr int SK_WARP = 6;                        // Sinkhorn, other gates, outputs
-constexpr int MIX_WARP0 = 7, NMIX = 9;            // x_in = sum_i H_pre[i] x[i]
+constexpr int SK_WARP0 = 6, NSK = 2;             // Sinkhorn, other gates, outputs (one per tile parity)
+constexpr int MIX_WARP0 = 8, NMIX = 8;            // x_in = sum_i H_pre[i] x[i]
+static_assert(GATE_WARP0 + NGATE == SK_WARP0 && SK_WARP0 + NSK == MIX_WARP0 && MIX_WARP0 + NMIX == NTHREADS / 32,
+              "warp roles: producer, MMA, gates, Sinkhorn, mix");
 // Token pieces a mix thread loads before it computes (4 streams x 16 B each).
 // Two keep the mix ahead of the tiles; four put so many L2 reads in flight
 // that the TMA stream's boxes land later and the whole kernel slows by 4%.
@@ -353,7 +355,7 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
             if (lane == 0) ptx::tc_commit(bar(BAR_ACC_FULL + tb));
             __syncwarp();
         }
-    } else if (warp < SK_WARP) {
+    } else if (warp < SK_WARP0) {
         // ------------------------------------------------- gates ----------
         // (1) TMEM -> this CTA's partial logits and sum of squares for every
         //     token row, pushed (st.async) to the CTA that reduces the token;
@@ -478,16 +480,19 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
                 if (lane < C) ptx::mbar_arrive_remote_relaxed(ptx::mapa(bar(BAR_RFREE), static_cast<uint32_t>(lane)));
             }
         }
-    } else if (warp == SK_WARP) {
+    } else if (warp < MIX_WARP0) {
         // ----------------------------------------- Sinkhorn and outputs ---
         // The other gates of this CTA's reduced tokens (H_post, Sinkhorn for
         // H_res) and every per-token output, off the mix's critical path.
-        // Eight lanes per token; lane l8 writes outputs l8 and l8 + 8 of the
-        // 13 float4-sized pieces: proj[0..5], inv_rms, H_pre, H_post, H_res[0..3].
+        // One warp per tile parity, so that a tile's Sinkhorn may take up to
+        // two tile periods (it grows with the round count).  Eight lanes per
+        // token; lane l8 writes outputs l8 and l8 + 8 of the 13 float4-sized
+        // pieces: proj[0..5], inv_rms, H_pre, H_post, H_res[0..3].
         const int l8 = lane & 7;
         int it = 0;
         for (int j = cid; j < p.ntiles; j += ncl, ++it) {
             const int tb = it & 1;
+            if (tb != warp - SK_WARP0) continue;
             const uint32_t use = static_cast<uint32_t>(it >> 1);
             if (!__all_sync(FULL, wait_bar<false>(bar(BAR_SKFULL + tb), use & 1, abort_flag))) break;
             const int64_t t0 = static_cast<int64_t>(j) * TILE_M;
