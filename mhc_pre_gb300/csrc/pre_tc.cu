@@ -67,6 +67,7 @@ cudaError_t set_force_timeout_pre(unsigned on) {
 cudaError_t read_and_clear_bwd_tc_error(unsigned* word);      // pre_bwd_tc.cu
 cudaError_t read_and_clear_bwd_fused_error(unsigned* word);   // pre_bwd_fused.cu
 cudaError_t read_and_clear_post_pre_error(unsigned* word);    // post_pre_tc.cu
+cudaError_t read_and_clear_post_norm_error(unsigned* word);   // post_norm.cu
 
 cudaError_t read_and_clear_device_error(unsigned* word, cudaStream_t s) {
     cudaError_t e = cudaStreamSynchronize(s);
@@ -86,6 +87,10 @@ cudaError_t read_and_clear_device_error(unsigned* word, cudaStream_t s) {
     *word |= other;
     other = 0;
     e = read_and_clear_post_pre_error(&other);
+    if (e != cudaSuccess) return e;
+    *word |= other;
+    other = 0;
+    e = read_and_clear_post_norm_error(&other);
     *word |= other;
     return e;
 }
