@@ -227,29 +227,50 @@ post_pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
     // phi slice -> bf16 hi / lo rows in the 64-byte-swizzled K-major layout
     // of the MMA's B operand: chunk ch = (pair, chunk of the slice, stream in
     // the pair), row n (< 24: hi of logit n, else lo), 16-byte piece q of the
-    // row at q ^ ((n >> 1) & 3).
-    for (int item = tid; item < nch * 4 * NG; item += NTHREADS) {
-        const int g = item % NG;
-        const int q = (item / NG) % 4;
-        const int ch = item / (NG * 4);
-        const int pr = ch / (2 * cpd), rem = ch % (2 * cpd);
-        const int sub = rem >> 1, i = 2 * pr + (rem & 1);
-        const int64_t k0 = static_cast<int64_t>(i) * D + static_cast<int64_t>(sub * C + c) * KW + q * 8;
-        uint32_t hi[4], lo[4];
+    // row at q ^ ((n >> 1) & 3).  Item (ch, q, g) is 8 consecutive K rows of
+    // logit g.  A thread issues the loads of all its items before it converts
+    // any, so that the set-up waits for one round trip to memory, not one per
+    // item.
+    {
+        constexpr int PHI_ITEMS = (MAX_NCH * 4 * NG + NTHREADS - 1) / NTHREADS;
+        const int nitems = nch * 4 * NG;
+        float v[PHI_ITEMS][8];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float v0 = p.phi[(k0 + 2 * e) * NG + g];
-            const float v1 = p.phi[(k0 + 2 * e + 1) * NG + g];
-            const __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
-            const float2 hf = __bfloat1622float2(h);
-            const __nv_bfloat162 l = __floats2bfloat162_rn(v0 - hf.x, v1 - hf.y);
-            hi[e] = *reinterpret_cast<const uint32_t*>(&h);
-            lo[e] = *reinterpret_cast<const uint32_t*>(&l);
+        for (int m = 0; m < PHI_ITEMS; ++m) {
+            const int item = tid + m * NTHREADS;
+            if (item < nitems) {
+                const int g = item % NG;
+                const int q = (item / NG) % 4;
+                const int ch = item / (NG * 4);
+                const int pr = ch / (2 * cpd), rem = ch % (2 * cpd);
+                const int sub = rem >> 1, i = 2 * pr + (rem & 1);
+                const int64_t k0 = static_cast<int64_t>(i) * D + static_cast<int64_t>(sub * C + c) * KW + q * 8;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[m][e] = p.phi[(k0 + e) * NG + g];
+            }
         }
-        unsigned char* chunk = smem + L.phi + ch * PHI_CHUNK_BYTES;
-        const int nh = g, nl = NG + g;
-        *reinterpret_cast<uint4*>(chunk + nh * ROW + ((q ^ ((nh >> 1) & 3)) * 16)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(chunk + nl * ROW + ((q ^ ((nl >> 1) & 3)) * 16)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+#pragma unroll
+        for (int m = 0; m < PHI_ITEMS; ++m) {
+            const int item = tid + m * NTHREADS;
+            if (item < nitems) {
+                const int g = item % NG;
+                const int q = (item / NG) % 4;
+                const int ch = item / (NG * 4);
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const __nv_bfloat162 h = __floats2bfloat162_rn(v[m][2 * e], v[m][2 * e + 1]);
+                    const float2 hf = __bfloat1622float2(h);
+                    const __nv_bfloat162 l = __floats2bfloat162_rn(v[m][2 * e] - hf.x, v[m][2 * e + 1] - hf.y);
+                    hi[e] = *reinterpret_cast<const uint32_t*>(&h);
+                    lo[e] = *reinterpret_cast<const uint32_t*>(&l);
+                }
+                unsigned char* chunk = smem + L.phi + ch * PHI_CHUNK_BYTES;
+                const int nh = g, nl = NG + g;
+                *reinterpret_cast<uint4*>(chunk + nh * ROW + ((q ^ ((nh >> 1) & 3)) * 16)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(chunk + nl * ROW + ((q ^ ((nl >> 1) & 3)) * 16)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+        }
     }
     ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();

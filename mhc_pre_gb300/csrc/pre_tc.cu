@@ -45,6 +45,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "launch.h"
@@ -57,11 +58,13 @@ namespace mhc {
 // mhc_get_last_device_error().
 __device__ unsigned g_device_error;
 // Test hook (mhc_test_force_timeout): nonzero makes pre_tc_kernel run one
-// bounded wait that nothing completes, then return.
-__device__ unsigned g_force_timeout_pre;
+// bounded wait that nothing completes, then return.  Passed to the kernel as
+// a launch parameter (no global read at the kernel's start).
+static std::atomic<unsigned> g_force_timeout_pre{0u};
 
 cudaError_t set_force_timeout_pre(unsigned on) {
-    return cudaMemcpyToSymbol(g_force_timeout_pre, &on, sizeof(unsigned));
+    g_force_timeout_pre.store(on);
+    return cudaSuccess;
 }
 
 cudaError_t read_and_clear_bwd_tc_error(unsigned* word);      // pre_bwd_tc.cu
@@ -171,6 +174,7 @@ struct Params {
     int D, Dc, nch, iters;
     float eps;
     int ntiles;
+    unsigned force_timeout;   // test hook
     __nv_bfloat16* x_in;
     float* H_pre;
     float* H_post;
@@ -216,7 +220,7 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
     const float* recv = reinterpret_cast<const float*>(smem + L.recv);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (g_force_timeout_pre != 0u) {
+    if (p.force_timeout != 0u) {
         // test hook: one bounded wait that runs out, before anything async
         // starts; every CTA of the launch takes this path and none touches a
         // peer, so leaving here is safe
@@ -256,8 +260,21 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
         }
         *abort_flag = 0;
         ptx::fence_mbar_init();
+        ptx::fence_proxy_async_smem();
+        // The first ring loads go out now, so that they are in flight while
+        // phi is staged (a fresh slot needs no wait); the producer loop below
+        // skips them.
+        ptx::prefetch_tmap(&tmap_x);
+        const uint64_t pol = ptx::policy_evict_normal();
+        const int first = ntl * (nch / 2) < STAGES ? ntl * (nch / 2) : STAGES;
+        for (int n = 0; n < first; ++n) {
+            const int j = cid + (n / (nch / 2)) * ncl, st = n % (nch / 2);
+            const int pr = st / cpd, sub = st % cpd;
+            ptx::mbar_arrive_expect_tx(bar(BAR_FULL + n), STAGE_BYTES);
+            ptx::tma_load_3d(sbase + L.stages + n * STAGE_BYTES, &tmap_x, (sub * C + static_cast<int>(c)) * KW,
+                             j * TILE_M, 2 * pr, bar(BAR_FULL + n), pol);
+        }
     }
-    if (warp == 0 && lane == 0) ptx::prefetch_tmap(&tmap_x);
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_slot), TMEM_COLS);
         ptx::tmem_relinquish();
@@ -266,31 +283,53 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
     if (tid >= 32 && tid < 32 + NG) gate_par[3 + tid - 32] = p.b[tid - 32];
     // phi slice -> bf16 hi / lo rows in the swizzled K-major layout of the
     // MMA's B operand: chunk ch, row n (< 24: hi of logit n, else lo of
-    // logit n - 24), 16-byte piece q of the row at (q ^ (n & 7)).
-    for (int item = tid; item < nch * 8 * NG; item += NTHREADS) {
-        const int g = item % NG;
-        const int q = (item / NG) % 8;
-        const int ch = item / (NG * 8);
-        // chunk order: stream pair, chunk of the slice, stream in the pair, so
-        // that the two phi chunks one stage needs are one 96-row B operand
-        const int pr = ch / (2 * cpd), rem = ch % (2 * cpd);
-        const int sub = rem >> 1, i = 2 * pr + (rem & 1);
-        const int64_t k0 = static_cast<int64_t>(i) * D + static_cast<int64_t>(sub * C + c) * KW + q * 8;
-        uint32_t hi[4], lo[4];
+    // logit n - 24), 16-byte piece q of the row at (q ^ (n & 7)).  Item
+    // (ch, q, g) is 8 consecutive K rows of logit g.  A thread issues the
+    // loads of all its items before it converts any, so that the set-up
+    // waits for one round trip to memory, not one per item.
+    {
+        constexpr int PHI_ITEMS = (MAX_NCH * 8 * NG + NTHREADS - 1) / NTHREADS;
+        const int nitems = nch * 8 * NG;
+        float v[PHI_ITEMS][8];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float v0 = p.phi[(k0 + 2 * e) * NG + g];
-            const float v1 = p.phi[(k0 + 2 * e + 1) * NG + g];
-            const __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
-            const float2 hf = __bfloat1622float2(h);
-            const __nv_bfloat162 l = __floats2bfloat162_rn(v0 - hf.x, v1 - hf.y);
-            hi[e] = *reinterpret_cast<const uint32_t*>(&h);
-            lo[e] = *reinterpret_cast<const uint32_t*>(&l);
+        for (int m = 0; m < PHI_ITEMS; ++m) {
+            const int item = tid + m * NTHREADS;
+            if (item < nitems) {
+                const int g = item % NG;
+                const int q = (item / NG) % 8;
+                const int ch = item / (NG * 8);
+                // chunk order: stream pair, chunk of the slice, stream in the
+                // pair, so that the two phi chunks one stage needs are one
+                // 96-row B operand
+                const int pr = ch / (2 * cpd), rem = ch % (2 * cpd);
+                const int sub = rem >> 1, i = 2 * pr + (rem & 1);
+                const int64_t k0 = static_cast<int64_t>(i) * D + static_cast<int64_t>(sub * C + c) * KW + q * 8;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[m][e] = p.phi[(k0 + e) * NG + g];
+            }
         }
-        unsigned char* chunk = smem + L.phi + ch * PHI_CHUNK_BYTES;
-        const int nh = g, nl = NG + g;
-        *reinterpret_cast<uint4*>(chunk + nh * 128 + ((q ^ (nh & 7)) * 16)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(chunk + nl * 128 + ((q ^ (nl & 7)) * 16)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+#pragma unroll
+        for (int m = 0; m < PHI_ITEMS; ++m) {
+            const int item = tid + m * NTHREADS;
+            if (item < nitems) {
+                const int g = item % NG;
+                const int q = (item / NG) % 8;
+                const int ch = item / (NG * 8);
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const __nv_bfloat162 h = __floats2bfloat162_rn(v[m][2 * e], v[m][2 * e + 1]);
+                    const float2 hf = __bfloat1622float2(h);
+                    const __nv_bfloat162 l = __floats2bfloat162_rn(v[m][2 * e] - hf.x, v[m][2 * e + 1] - hf.y);
+                    hi[e] = *reinterpret_cast<const uint32_t*>(&h);
+                    lo[e] = *reinterpret_cast<const uint32_t*>(&l);
+                }
+                unsigned char* chunk = smem + L.phi + ch * PHI_CHUNK_BYTES;
+                const int nh = g, nl = NG + g;
+                *reinterpret_cast<uint4*>(chunk + nh * 128 + ((q ^ (nh & 7)) * 16)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(chunk + nl * 128 + ((q ^ (nl & 7)) * 16)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+        }
     }
     ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
@@ -304,11 +343,16 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
         // ------------------------------------------------ TMA producer ----
         // The whole warp walks the loop; lane 0 waits and issues.
         const uint64_t pol = ptx::policy_evict_normal();
-        int stage = 0;
+        const int first = ntl * (nch / 2) < STAGES ? ntl * (nch / 2) : STAGES;   // issued at set-up
+        int stage = 0, n = 0;
         uint32_t round = 0;
         for (int j = cid; j < p.ntiles; j += ncl) {
             const int t0 = j * TILE_M;
-            for (int st = 0; st < nch / 2; ++st) {
+            for (int st = 0; st < nch / 2; ++st, ++n) {
+                if (n < first) {
+                    if (++stage == STAGES) { stage = 0; ++round; }
+                    continue;
+                }
                 const int pr = st / cpd, sub = st % cpd;       // stream pair, chunk of the slice
                 const int xd = (sub * C + static_cast<int>(c)) * KW;   // chunks interleaved over the cluster
                 bool ok = true;
@@ -758,6 +802,7 @@ cudaError_t launch_pre_tc(const void* x, const float* phi, const float* b, const
     prm.iters = iters;
     prm.eps = eps;
     prm.ntiles = static_cast<int>((T + tc::TILE_M - 1) / tc::TILE_M);
+    prm.force_timeout = g_force_timeout_pre.load();
     prm.x_in = static_cast<__nv_bfloat16*>(x_in);
     prm.H_pre = H_pre;
     prm.H_post = H_post;
