@@ -195,14 +195,16 @@ mhc_status mhc_post_bwd(mhc_dtype dt, const void* g_next, const void* x,
 
 /*
  * mhc_test_force_timeout -- test hook of the failure path, off by default.
- * While on (nonzero), every launch of the bf16 tensor-core forward kernel
- * (mhc_pre, mhc_pre_gates) and of the pre backward's one-pass cluster kernel
- * (mhc_pre_bwd) makes thread 0 of each CTA wait on an mbarrier that nothing
- * arrives on; the wait gives up after about 100 us, the kernel latches its
- * device error word and returns before starting any copy or tensor-memory
- * allocation, leaving its outputs unwritten.  The next
+ * While on (nonzero), every launch of the bf16 forward kernels (the
+ * tensor-core kernel and the small-batch cluster kernel of mhc_pre,
+ * mhc_pre_gates and mhc_pre_critical) and of the pre backward's one-pass
+ * cluster kernel (mhc_pre_bwd) makes thread 0 of each CTA wait on an mbarrier
+ * that nothing arrives on; the wait gives up after about 100 us, the kernel
+ * latches its device error word and returns before starting any copy or
+ * tensor-memory allocation, leaving its outputs unwritten.  The next
  * mhc_get_last_device_error() then reports MHC_ERR_TIMEOUT, and the context
- * stays usable.  Synchronous (it writes a device flag); applies to the
+ * stays usable.  Synchronous for the backward (it writes a device flag); the
+ * forward kernels take the setting as a launch parameter.  Applies to the
  * current device.  Not for production use.
  */
 mhc_status mhc_test_force_timeout(int on);

@@ -21,7 +21,7 @@ LIB = os.path.join(HERE, "libmhc_gb300.so")
 SOURCES = ["mhc_abi.cu", "kernels_fwd.cu", "kernels_bwd.cu", "pre_tc.cu", "pre_bwd_tc.cu",
            "pre_bwd_fused.cu",
            "pre_bwd_noalloc.cu", "post_pre_tc.cu",
-           "post_norm.cu"]
+           "post_norm.cu", "pre_small.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
          "--expt-relaxed-constexpr", "-Xptxas", "-warn-spills"]

@@ -71,6 +71,11 @@ cudaError_t read_and_clear_bwd_tc_error(unsigned* word);      // pre_bwd_tc.cu
 cudaError_t read_and_clear_bwd_fused_error(unsigned* word);   // pre_bwd_fused.cu
 cudaError_t read_and_clear_post_pre_error(unsigned* word);    // post_pre_tc.cu
 cudaError_t read_and_clear_post_norm_error(unsigned* word);   // post_norm.cu
+cudaError_t read_and_clear_small_error(unsigned* word);       // pre_small.cu
+bool pre_small_supports(int64_t T, int64_t D);                 // pre_small.cu
+cudaError_t launch_pre_small(const void* x, const float* phi, const float* b, const float* alpha, int64_t T,
+                             int64_t D, int iters, float eps, void* x_in, float* H_pre, float* H_post,
+                             float* H_res, float* proj, float* inv_rms, unsigned force_timeout, cudaStream_t s);
 
 cudaError_t read_and_clear_device_error(unsigned* word, cudaStream_t s) {
     cudaError_t e = cudaStreamSynchronize(s);
@@ -94,6 +99,10 @@ cudaError_t read_and_clear_device_error(unsigned* word, cudaStream_t s) {
     *word |= other;
     other = 0;
     e = read_and_clear_post_norm_error(&other);
+    if (e != cudaSuccess) return e;
+    *word |= other;
+    other = 0;
+    e = read_and_clear_small_error(&other);
     *word |= other;
     return e;
 }
@@ -775,6 +784,10 @@ cudaError_t launch_pre_tc(const void* x, const float* phi, const float* b, const
                           int64_t T, int64_t D, int iters, float eps, void* x_in, float* H_pre,
                           float* H_post, float* H_res, float* proj, float* inv_rms,
                           cudaStream_t s) {
+    // a few tokens: the cluster split-K kernel without the tensor-core ring
+    if (pre_small_supports(T, D))
+        return launch_pre_small(x, phi, b, alpha, T, D, iters, eps, x_in, H_pre, H_post, H_res, proj, inv_rms,
+                                g_force_timeout_pre.load(), s);
     const int C = tc::cluster_for(D);
     auto encode = tc::encode_fn();
     if (C == 0 || encode == nullptr) return cudaErrorNotSupported;

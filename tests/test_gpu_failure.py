@@ -68,3 +68,30 @@ def test_forced_timeout_is_reported_and_the_context_stays_usable():
         assert torch.equal(getattr(f, k), getattr(ref_f, k)), k
     for k in ("dx", "dphi", "db", "dalpha"):
         assert torch.equal(getattr(qb, k), getattr(ref_b, k)), k
+
+
+def test_forced_timeout_in_the_small_batch_forward():
+    """Two tokens take the cluster split-K forward for small batches: its
+    bounded wait gives up under the same hook, the status is reported, and
+    the next call gives the first run's outputs bit for bit."""
+    dev = _dev()
+    L = B.lib()
+    w = W.WORKLOADS[4].with_(T=2, D=5120, wid=82)
+    inp = W.make_inputs(w, device=dev)
+    x, phi, b, alpha = inp["x"], inp["phi"], inp["b"], inp["alpha"]
+    ref = B.mhc_pre(x, phi, b, alpha, w.iters, w.eps)
+    torch.cuda.synchronize()
+    assert B.get_last_device_error() == B.MHC_OK
+    try:
+        assert L.mhc_test_force_timeout(1) == B.MHC_OK
+        t0 = time.monotonic()
+        B.mhc_pre(x, phi, b, alpha, w.iters, w.eps)
+        assert B.get_last_device_error() == B.MHC_ERR_TIMEOUT
+        assert time.monotonic() - t0 < 30.0
+    finally:
+        assert L.mhc_test_force_timeout(0) == B.MHC_OK
+    f = B.mhc_pre(x, phi, b, alpha, w.iters, w.eps)
+    torch.cuda.synchronize()
+    assert B.get_last_device_error() == B.MHC_OK
+    for k in ("x_in", "H_pre", "H_post", "H_res", "proj", "inv_rms"):
+        assert torch.equal(getattr(f, k), getattr(ref, k)), k
