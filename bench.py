@@ -633,14 +633,14 @@ def graph_latency_us(fn, dev, calls=20, reps=7):
 
 
 def run_decode(w, dev):
-    """Decode-sized batches (T = 1, 8, 64 at the workload's width): latency of
+    """Decode-sized batches (T = 1, 8, 32, 64 at the workload's width): latency of
     mhc_pre, of the inference critical path (mhc_pre_critical: x_in, H_pre,
     saved state) and of its side (mhc_post_res_gates: H_post, H_res with
     Sinkhorn, which a second stream overlaps with the sublayer)."""
     from mhc_pre_gb300 import binding as B
     from mhc_pre_gb300 import workloads as W
     out = {}
-    for T in (1, 8, 64):
+    for T in (1, 8, 32, 64):
         wd = w.with_(T=T, backward=False)
         inp = W.make_inputs(wd, device=dev)
         x, phi, b, alpha = inp["x"], inp["phi"], inp["b"], inp["alpha"]

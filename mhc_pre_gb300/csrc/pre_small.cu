@@ -1,5 +1,5 @@
 // pre_small.cu -- the pre forward of the mHC layer for decode-sized batches
-// (bf16, at most eight tokens).
+// (bf16, at most 56 tokens: one cluster per eight).
 //
 // What it computes is the same per-token map as the tensor-core kernel
 // (section 5.3 of the "openPangu 2.0 -- architecture, training and Ascend
@@ -10,7 +10,8 @@
 // At a few tokens the work is reading phi (4*D x 24 floats, 1.97 MB at
 // D = 5120) and a chain of latencies; the tensor-core kernel's ring of
 // 64-token boxes and its eight MMAs per stage only add to that chain.  Here
-// one cluster of 16 CTAs (one per SM) splits K:
+// one cluster of 16 CTAs (one per SM) per eight tokens splits K (each cluster
+// reads all of phi; the later ones from L2):
 //   * CTA c brings its K-slice of phi (fp32, contiguous) into shared memory
 //     with one bulk copy, and the tokens' matching slices of x with plain
 //     loads by every thread meanwhile (one bulk copy per token made each
@@ -31,6 +32,8 @@
 // cluster barriers (the call's outputs are then not valid).
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <mutex>
 
 #include "launch.h"
 #include "mhc_common.cuh"
@@ -53,7 +56,8 @@ namespace sm {
 constexpr int CS = 16;                 // CTAs of the cluster
 constexpr int NT = 512;                // 16 warps
 constexpr int NW = NT / 32;
-constexpr int TMAX = 8;                // tokens
+constexpr int TMAX = 8;                // tokens per cluster
+constexpr int TCAP = 56;               // tokens per launch (one cluster per TMAX)
 constexpr int PF = 28;                 // partial record: 24 logits, sum of x^2, pad (floats)
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;   // 1 s
 
@@ -94,9 +98,19 @@ struct Layout {
 };
 
 template <int RP>
-__global__ void __launch_bounds__(NT, 1) pre_small_kernel(const Params p) {
+__global__ void __launch_bounds__(NT, 1) pre_small_kernel(const Params batch) {
     extern __shared__ __align__(128) unsigned char smem[];
-    const int D = p.D, T = p.T;
+    // cluster j takes tokens [TMAX j, TMAX j + T) of the batch
+    const int j0 = static_cast<int>(ptx::cluster_id_x()) * TMAX;
+    Params p = batch;
+    p.x += static_cast<int64_t>(j0) * 4 * p.D;
+    if (p.x_in != nullptr) p.x_in += static_cast<int64_t>(j0) * p.D;
+    p.H_pre += j0 * 4;
+    if (p.H_post != nullptr) p.H_post += j0 * 4;
+    if (p.H_res != nullptr) p.H_res += j0 * 16;
+    p.proj += j0 * NG;
+    p.inv_rms += j0;
+    const int D = p.D, T = min(TMAX, batch.T - j0);
     const int KS = D / 4;
     const int64_t K = 4ll * D;
     const Layout L = Layout::make(D);
@@ -274,14 +288,57 @@ __global__ void __launch_bounds__(NT, 1) pre_small_kernel(const Params p) {
 
 }  // namespace sm
 
+// Clusters of the small-batch kernel that can be resident at once at width D,
+// per device.  The clusters of a launch are independent (each reads all of
+// phi); the path is taken only when they all fit at once, so that a batch
+// costs one cluster's latency.
+int small_clusters_resident(int64_t D) {
+    static std::mutex mu;
+    static int cached_dev[8] = {-1, -1, -1, -1, -1, -1, -1, -1};
+    static int64_t cached_D[8];
+    static int cached_n[8];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < 8; ++i)
+        if (cached_dev[i] == dev && cached_D[i] == D) return cached_n[i];
+    const size_t smem = sm::Layout::make(static_cast<int>(D)).total;
+    auto k = sm::pre_small_kernel<1>;
+    int n = 0;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) == cudaSuccess &&
+        cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(sm::CS * 16);
+        cfg.blockDim = dim3(sm::NT);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = sm::CS;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) n = 0;
+    }
+    for (int i = 0; i < 8; ++i)
+        if (cached_dev[i] < 0) {
+            cached_dev[i] = dev;
+            cached_D[i] = D;
+            cached_n[i] = n;
+            break;
+        }
+    return n;
+}
+
 bool pre_small_supports(int64_t T, int64_t D) {
-    if (T < 1 || T > sm::TMAX || D <= 0 || D % 512 != 0) return false;
+    if (T < 1 || T > sm::TCAP || D <= 0 || D % 512 != 0) return false;
     int dev = 0, optin = 0, cl = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&cl, cudaDevAttrClusterLaunch, dev) != cudaSuccess || cl == 0)
         return false;
-    return sm::Layout::make(static_cast<int>(D)).total <= static_cast<uint32_t>(optin);
+    if (sm::Layout::make(static_cast<int>(D)).total > static_cast<uint32_t>(optin)) return false;
+    return small_clusters_resident(D) >= static_cast<int>((T + sm::TMAX - 1) / sm::TMAX);
 }
 
 cudaError_t launch_pre_small(const void* x, const float* phi, const float* b, const float* alpha, int64_t T,
@@ -292,7 +349,7 @@ cudaError_t launch_pre_small(const void* x, const float* phi, const float* b, co
     void (*k)(sm::Params) = T <= 1 ? sm::pre_small_kernel<8>
                           : T <= 2 ? sm::pre_small_kernel<4>
                           : T <= 4 ? sm::pre_small_kernel<2>
-                                   : sm::pre_small_kernel<1>;
+                                   : sm::pre_small_kernel<1>;   // clusters of eight tokens
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
@@ -313,7 +370,7 @@ cudaError_t launch_pre_small(const void* x, const float* phi, const float* b, co
     prm.proj = proj;
     prm.inv_rms = inv_rms;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(sm::CS);
+    cfg.gridDim = dim3(static_cast<unsigned>(sm::CS * ((T + sm::TMAX - 1) / sm::TMAX)));
     cfg.blockDim = dim3(sm::NT);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;

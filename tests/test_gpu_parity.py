@@ -68,9 +68,10 @@ def test_workload4_bf16_fwd_bwd_s4096():
     (1, 4, "f32"), (67, 12, "f32"), (130, 260, "f32"),
     # fewer tokens than one 64-token tile (decode-sized batches)
     (2, 5120, "bf16"), (17, 5120, "bf16"), (63, 2560, "bf16"), (5, 1024, "bf16"),
-    # the split-K cluster kernel of at most eight tokens (widths a multiple of
-    # 512), its edges, and the first batch past it
+    # the split-K cluster kernel (one cluster per eight tokens, at most 56
+    # tokens, widths a multiple of 512), its edges, and the first batch past it
     (8, 5120, "bf16"), (8, 512, "bf16"), (4, 6144, "bf16"), (3, 2560, "bf16"), (9, 5120, "bf16"),
+    (32, 5120, "bf16"), (26, 1024, "bf16"), (56, 5120, "bf16"), (57, 5120, "bf16"),
     # widths past the cluster kernels' (a phi slice of at most 1280 columns per
     # CTA): the CUDA-core forward, and the two-pass tensor-core backward from
     # one 128-token tile up
