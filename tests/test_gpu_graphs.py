@@ -100,3 +100,43 @@ def test_recompute_backward_in_a_cuda_graph_matches_eager():
     assert B.get_last_device_error() == B.MHC_OK
     for e, o in zip(eager, out):
         assert torch.equal(e, o)
+
+
+_SMALL_BATCH_CAPTURE_SCRIPT = r"""
+import torch
+from mhc_pre_gb300 import binding as B
+from mhc_pre_gb300 import workloads as W
+
+dev = torch.device("cuda", 0)
+torch.cuda.set_device(dev)
+w = W.WORKLOADS[5].with_(T=4, backward=False)
+a = W.make_inputs(w, device=dev)
+s = torch.cuda.Stream(dev)
+s.wait_stream(torch.cuda.current_stream(dev))
+g = torch.cuda.CUDAGraph()
+# the first small-batch call of the process is made inside the capture
+with torch.cuda.graph(g, stream=s):
+    f = B.mhc_pre(a["x"], a["phi"], a["b"], a["alpha"], w.iters, w.eps)
+g.replay()
+torch.cuda.synchronize()
+e = B.mhc_pre(a["x"], a["phi"], a["b"], a["alpha"], w.iters, w.eps)
+torch.cuda.synchronize()
+same = all(torch.equal(getattr(f, k), getattr(e, k)) for k in ("x_in", "H_pre", "H_post", "H_res", "proj", "inv_rms"))
+print("RESULT", int(same), B.get_last_device_error())
+"""
+
+
+def test_small_batch_forward_captured_as_the_first_call():
+    """In a fresh process, the first call of the small-batch forward (T = 4)
+    happens inside a CUDA-graph capture, where the library looks up its
+    cluster occupancy: the replayed graph gives the eager call's bits."""
+    import os
+    import subprocess
+    import sys
+    _dev()
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _SMALL_BATCH_CAPTURE_SCRIPT], cwd=root, capture_output=True,
+                       text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = [l for l in r.stdout.splitlines() if l.startswith("RESULT")][-1]
+    assert line.split()[1:] == ["1", str(B.MHC_OK)], line
