@@ -121,3 +121,27 @@ def test_first_call_while_capturing_is_refused():
     assert r.returncode == 0, r.stderr[-2000:]
     line = [l for l in r.stdout.splitlines() if l.startswith("STATUS")][-1]
     assert line.split()[1:] == [str(B.MHC_ERR_UNSUPPORTED), str(B.MHC_OK), str(B.MHC_OK)], line
+
+
+@pytest.mark.parametrize("wid,T,D,dtype", [(76, 333, 2560, "bf16"), (77, 64, 256, "f32")])
+def test_noalloc_against_the_oracle(wid, T, D, dtype):
+    """The layer's backward with mhc_pre_bwd_noalloc in place of mhc_pre_bwd,
+    element by element against the float64 oracle (the same tolerances as
+    the parity tests), so that this entry point is pinned to the oracle
+    directly and not only through the workspace entry point."""
+    import numpy as np
+    dev = _dev()
+    w = W.WORKLOADS[4].with_(T=T, D=D, dtype=dtype, wid=wid, backward=True)
+    cpu = W.make_inputs(w, device="cpu")
+    inp = {k: v.to(dev) for k, v in cpu.items()}
+    ref = P.run_oracle({k: P.f64(v) for k, v in cpu.items()}, w.iters, w.eps, True)
+    x, phi, b, alpha = inp["x"], inp["phi"], inp["b"], inp["alpha"]
+    f = B.mhc_pre(x, phi, b, alpha, w.iters, w.eps)
+    pb = B.mhc_post_bwd(inp["g_next"], x, inp["y"], f.H_post, f.H_res)
+    qb = B.mhc_pre_bwd_noalloc(inp["g_in"], pb.dH_post, pb.dH_res, x, phi, b, alpha, f.proj, f.inv_rms,
+                               pb.dx, w.iters)
+    torch.cuda.synchronize()
+    assert B.get_last_device_error() == B.MHC_OK
+    got = dict(dx=qb.dx, dphi=qb.dphi, db=qb.db, dalpha=qb.dalpha)
+    P.compare(got, ref, fp32=(dtype == "f32"), keys=("dx", "dphi", "db", "dalpha"))
+    assert np.isfinite(P.f64(qb.dphi)).all()
