@@ -14,8 +14,7 @@
 // reads all of phi; the later ones from L2):
 //   * CTA c brings its K-slice of phi (fp32, contiguous) into shared memory
 //     with one bulk copy, and the tokens' matching slices of x with plain
-//     loads by every thread meanwhile (one bulk copy per token made each
-//     token cost about a microsecond more);
+//     loads by every thread meanwhile;
 //   * each warp takes 1/16 of the slice's rows; lane (token, group of six
 //     logits, row phase) accumulates in fp32, and for one logit group the
 //     token's squares;
@@ -24,10 +23,11 @@
 //     the CTA that owns the token, which adds the 16 partials in CTA order,
 //     forms inv_rms, proj and H_pre and broadcasts H_pre to the cluster;
 //   * after a second cluster barrier every CTA mixes its share of the
-//     columns, and the owners write the saved state and the other gates.
+//     columns (warps 1..15) while warp 0 of each owner runs the other gates
+//     and Sinkhorn.
 // Every sum runs in a fixed order, so results do not depend on timing, and
 // mhc_pre, mhc_pre_gates and mhc_pre_critical agree bit for bit.  The one
-// wait on the bulk copies is bounded (about a second); on expiry the kernel
+// wait, on phi's bulk copy, is bounded (about a second); on expiry the kernel
 // latches its device error word and skips its work, still passing both
 // cluster barriers (the call's outputs are then not valid).
 #include <cuda_runtime.h>
@@ -253,7 +253,9 @@ __global__ void __launch_bounds__(NT, 1) pre_small_kernel(const Params batch) {
         const float4* hb = reinterpret_cast<const float4*>(smem + L.hpre);
         const int qpt = D / 8;                         // pieces per stream row
         const int per = (qpt - static_cast<int>(c) + CS - 1) / CS;
-        for (int item = tid; item < T * per; item += NT) {
+        // warps 1.. only: warp 0 of a token's owner runs Sinkhorn meanwhile
+        for (int item = tid - 32; item < T * per; item += NT - 32) {
+            if (item < 0) break;
             const int t = item / per, qq = static_cast<int>(c) + (item % per) * CS;
             const __nv_bfloat16* src = p.x + t * K + qq * 8;
             uint4 xv[4];
@@ -282,6 +284,12 @@ __global__ void __launch_bounds__(NT, 1) pre_small_kernel(const Params batch) {
             for (int v4 = 1; v4 < 4; ++v4)
                 if (r == v4) o = make_float4(hr[4 * v4], hr[4 * v4 + 1], hr[4 * v4 + 2], hr[4 * v4 + 3]);
             reinterpret_cast<float4*>(p.H_res + static_cast<int64_t>(t_own) * 16)[r] = o;
+        }
+    }
+    if (!ok) {
+        // let a copy still in flight land before the shared memory goes away
+        const uint64_t t0 = ptx::globaltimer();
+        while (ptx::globaltimer() - t0 < 20000ull) {
         }
     }
 }
