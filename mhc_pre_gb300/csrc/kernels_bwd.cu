@@ -386,9 +386,20 @@ pre_bwd_reduce_phi_kernel(const float* __restrict__ part, int64_t nb, int64_t n4
                           float* __restrict__ db, float* __restrict__ dalpha) {
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        float4 s = reinterpret_cast<const float4*>(part)[i];
-        for (int64_t bb = 1; bb < nb; ++bb) {
-            const float4 v = reinterpret_cast<const float4*>(part)[bb * n4 + i];
+        // the partials' loads go out four at a time (one round trip per four
+        // blocks, not per block); the sum keeps block order
+        const float4* pp = reinterpret_cast<const float4*>(part) + i;
+        float4 s = pp[0];
+        int64_t bb = 1;
+        for (; bb + 4 <= nb; bb += 4) {
+            const float4 v0 = pp[bb * n4], v1 = pp[(bb + 1) * n4], v2 = pp[(bb + 2) * n4], v3 = pp[(bb + 3) * n4];
+            s.x += v0.x; s.y += v0.y; s.z += v0.z; s.w += v0.w;
+            s.x += v1.x; s.y += v1.y; s.z += v1.z; s.w += v1.w;
+            s.x += v2.x; s.y += v2.y; s.z += v2.z; s.w += v2.w;
+            s.x += v3.x; s.y += v3.y; s.z += v3.z; s.w += v3.w;
+        }
+        for (; bb < nb; ++bb) {
+            const float4 v = pp[bb * n4];
             s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
         }
         reinterpret_cast<float4*>(dphi)[i] = s;
@@ -418,6 +429,8 @@ pre_bwd_bias_partial_kernel(const float* __restrict__ rec, int64_t T, float* __r
     const int k = lane / 7, v = lane - 7 * (lane / 7);   // token slot, piece
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (lane < 28) {
+        // loads of four token rows per round trip; the sum keeps token order
+#pragma unroll 4
         for (int64_t t = t_begin + warp * 4 + k; t < t_end; t += 32) {
             const float4 a = reinterpret_cast<const float4*>(rec + t * REC + REC_DL)[v];
             acc.x += a.x; acc.y += a.y; acc.z += a.z; acc.w += a.w;
