@@ -582,6 +582,145 @@ post_norm_bwd_staged_kernel(const __nv_bfloat16* __restrict__ g_next, const __nv
     }
 }
 
+// ---- staged forward (bf16 rows that fit in shared memory) ----------------
+// A token's x and y rows (10 D bytes) arrive in shared memory by bulk copies
+// into one of two buffers, the next token's while this one is worked, so the
+// statistics passes (sum of y^2, sum of z^2) and the store pass read them on
+// chip instead of the store pass re-reading x from L2.  Two CTAs per SM.
+// The per-element expressions are those of the kernel above (with no step,
+// x_next is mhc_post's bit for bit); the row sums run over this CTA shape.
+template <int NT, int flags>
+__global__ void __launch_bounds__(NT, 2)
+post_norm_fwd_staged_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ y,
+                            const float* __restrict__ H_post, const float* __restrict__ H_res, float eps, int64_t T,
+                            int64_t D, __nv_bfloat16* __restrict__ x_next, float* __restrict__ inv_rms_y,
+                            float* __restrict__ inv_rms_out) {
+    using TA = __nv_bfloat16;
+    constexpr int V = 8;
+    extern __shared__ __align__(128) unsigned char stage[];   // 2 x [x 4D | y D]
+    __shared__ float red[NT / 32];
+    __shared__ __align__(8) uint64_t full[2];
+    const int tid = threadIdx.x;
+    const int64_t QD = D / V;
+    const int64_t G = gridDim.x;
+    const uint32_t buf_bytes = static_cast<uint32_t>(10 * D);
+    const uint32_t sb = ptx::smem_u32(stage);
+    const uint32_t bar0 = ptx::smem_u32(&full[0]);
+    if (tid == 0) {
+        ptx::mbar_init(bar0, 1);
+        ptx::mbar_init(bar0 + 8, 1);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    // thread 0: token t's two rows into buffer b
+    auto issue = [&](int b, int64_t t) {
+        const uint32_t bar = bar0 + 8u * static_cast<uint32_t>(b);
+        const uint32_t dst = sb + static_cast<uint32_t>(b) * buf_bytes;
+        ptx::mbar_arrive_expect_tx(bar, buf_bytes);
+        ptx::bulk_load(dst, x + t * 4 * D, static_cast<uint32_t>(8 * D), bar);
+        ptx::bulk_load(dst + static_cast<uint32_t>(8 * D), y + t * D, static_cast<uint32_t>(2 * D), bar);
+    };
+    if (tid == 0) {
+        for (int b = 0; b < 2; ++b)
+            if (blockIdx.x + b * G < T) issue(b, blockIdx.x + b * G);
+    }
+    bool aborted = false;
+    int k = 0;
+    for (int64_t t = blockIdx.x; t < T; t += G, ++k) {
+        const int b = k & 1;
+        const Gates g = load_gates(H_post, H_res, t);
+        bool timed_out = false;
+        {
+            const uint32_t bar = bar0 + 8u * static_cast<uint32_t>(b), par = static_cast<uint32_t>(k >> 1) & 1u;
+            if (!ptx::mbar_try_wait(bar, par)) {
+                const uint64_t t0 = ptx::globaltimer();
+                while (!ptx::mbar_try_wait(bar, par)) {
+                    if (ptx::globaltimer() - t0 > STG_WAIT_NS) {
+                        timed_out = true;
+                        break;
+                    }
+                }
+            }
+        }
+        if (__syncthreads_or(timed_out)) {
+            if (tid == 0) atomicOr(&g_post_norm_error, 1u);
+            aborted = true;
+            break;
+        }
+        const TA* xs = reinterpret_cast<const TA*>(stage + static_cast<size_t>(b) * buf_bytes);
+        const TA* ys = xs + 4 * D;
+        float ry = 1.0f;
+        if constexpr ((flags & SANDWICH) != 0) {
+            float ssq = 0.f;
+#pragma unroll 2
+            for (int64_t q = tid; q < QD; q += NT) {
+                float yv[V];
+                Vec<TA>::unpack(*reinterpret_cast<const uint4*>(ys + q * V), yv);
+#pragma unroll
+                for (int e = 0; e < V; ++e) ssq = fmaf(yv[e], yv[e], ssq);
+            }
+            ry = 1.0f / sqrtf(block_sum<NT>(ssq, red) / static_cast<float>(D) + eps);
+        }
+        float s = 1.0f;
+        if constexpr ((flags & BLOCK) != 0) {
+            float zz = 0.f;
+#pragma unroll 2
+            for (int64_t q = tid; q < QD; q += NT) {
+                float yv[V], f[4][V];
+                Vec<TA>::unpack(*reinterpret_cast<const uint4*>(ys + q * V), yv);
+#pragma unroll
+                for (int e = 0; e < V; ++e) yv[e] *= ry;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) Vec<TA>::unpack(*reinterpret_cast<const uint4*>(xs + j * D + q * V), f[j]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int e = 0; e < V; ++e) {
+                        const float z = post_elem(g, i, f[0][e], f[1][e], f[2][e], f[3][e], yv[e]);
+                        zz = fmaf(z, z, zz);
+                    }
+            }
+            s = 1.0f / sqrtf(block_sum<NT>(zz, red) / static_cast<float>(4 * D) + eps);
+        }
+#pragma unroll 2
+        for (int64_t q = tid; q < QD; q += NT) {
+            float yv[V], f[4][V];
+            Vec<TA>::unpack(*reinterpret_cast<const uint4*>(ys + q * V), yv);
+            if constexpr ((flags & SANDWICH) != 0) {
+#pragma unroll
+                for (int e = 0; e < V; ++e) yv[e] *= ry;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) Vec<TA>::unpack(*reinterpret_cast<const uint4*>(xs + j * D + q * V), f[j]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float o[V];
+#pragma unroll
+                for (int e = 0; e < V; ++e) {
+                    const float z = post_elem(g, i, f[0][e], f[1][e], f[2][e], f[3][e], yv[e]);
+                    o[e] = ((flags & BLOCK) != 0) ? z * s : z;
+                }
+                st16_stream(x_next + t * 4 * D + i * D + q * V, Vec<TA>::pack(o));
+            }
+        }
+        // this thread is done with the buffer; the barrier orders every
+        // thread's reads before the next bulk copy into it
+        ptx::fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            if (t + 2 * G < T) issue(b, t + 2 * G);
+            inv_rms_y[t] = ry;
+            inv_rms_out[t] = s;
+        }
+    }
+    if (aborted) {
+        // let copies already issued land before the shared memory goes away
+        const uint64_t t0 = ptx::globaltimer();
+        while (ptx::globaltimer() - t0 < 20000ull) {
+        }
+    }
+}
+
 // CTAs per launch: `per_sm` for every SM, at most one per token.
 int grid_for(int64_t T, int per_sm) {
     int dev = 0, n = 0;
@@ -603,6 +742,27 @@ void fwd(const void* x, const void* y, const float* H_post, const float* H_res, 
     post_norm_kernel<TA, F><<<grid_for(T, 16), FWD_NT, 0, s>>>(
         static_cast<const TA*>(x), static_cast<const TA*>(y), H_post, H_res, eps, T, D, static_cast<TA*>(x_next),
         inv_rms_y, inv_rms_out);
+}
+
+// The staged forward: bf16 rows whose two buffers (20 D bytes) fit.
+constexpr int STGF_NT = 256;
+size_t staged_smem_limit();
+
+bool staged_fwd_supports(bool bf16, int64_t D) {
+    return bf16 && D % 8 == 0 && static_cast<size_t>(20 * D) <= staged_smem_limit();
+}
+
+template <int F>
+cudaError_t fwd_staged(const void* x, const void* y, const float* H_post, const float* H_res, float eps, int64_t T,
+                       int64_t D, void* x_next, float* inv_rms_y, float* inv_rms_out, cudaStream_t s) {
+    auto k = post_norm_fwd_staged_kernel<STGF_NT, F>;
+    const size_t smem = static_cast<size_t>(20 * D);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    using B = __nv_bfloat16;
+    k<<<grid_for(T, 2), STGF_NT, smem, s>>>(static_cast<const B*>(x), static_cast<const B*>(y), H_post, H_res, eps,
+                                            T, D, static_cast<B*>(x_next), inv_rms_y, inv_rms_out);
+    return cudaGetLastError();
 }
 
 // Buffers per CTA of the staged backward (CTAs per SM: 3 - STG_NBUF) and its
@@ -660,6 +820,17 @@ bool post_norm_supports(bool bf16, int64_t D) { return post_norm_supports_impl(b
 cudaError_t launch_post_norm(bool bf16, const void* x, const void* y, const float* H_post, const float* H_res,
                              int flags, float eps, int64_t T, int64_t D, void* x_next, float* inv_rms_y,
                              float* inv_rms_out, cudaStream_t s) {
+    if (staged_fwd_supports(bf16, D)) {
+#define MHC_PN_STGF(F) fwd_staged<F>(x, y, H_post, H_res, eps, T, D, x_next, inv_rms_y, inv_rms_out, s)
+        switch (flags) {
+            case 0: return MHC_PN_STGF(0);
+            case 1: return MHC_PN_STGF(1);
+            case 2: return MHC_PN_STGF(2);
+            case 3: return MHC_PN_STGF(3);
+        }
+#undef MHC_PN_STGF
+        return cudaErrorInvalidValue;
+    }
 #define MHC_PN_FWD(TA, F) fwd<TA, F>(x, y, H_post, H_res, eps, T, D, x_next, inv_rms_y, inv_rms_out, s)
     switch (flags + (bf16 ? 4 : 0)) {
         case 0: MHC_PN_FWD(float, 0); break;
