@@ -174,23 +174,26 @@ pre_bwd_token_kernel(const float* __restrict__ dH_post, const float* __restrict_
 
     const float s = inv_rms[t];
     const float a[3] = {alpha[0], alpha[1], alpha[2]};
-    float vp = 0.f, da[3] = {0.f, 0.f, 0.f};
+    float vp = 0.f, da[3] = {0.f, 0.f, 0.f}, u[NG];
 #pragma unroll
     for (int g = 0; g < NG; ++g) {
         const int grp = group_of(g);
         const float v = a[grp] * dl[g];
         vp = fmaf(v, pj[g], vp);
         da[grp] = fmaf(dl[g], pj[g], da[grp]);
-        r[REC_U + g] = s * v;
-        r[REC_DL + g] = dl[g];
+        u[g] = s * v;
     }
+    // the record in 16-byte pieces (slots 30, 31 and 59 are unused)
+    float4* r4 = reinterpret_cast<float4*>(r);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) r[REC_HPRE + i] = hpre[i];
-    r[REC_COEF] = -s * s * vp / static_cast<float>(K);
-    r[REC_S] = s;
-    reinterpret_cast<float4*>(r + REC_DSIG)[0] = make_float4(dsig[0], dsig[1], dsig[2], dsig[3]);
-#pragma unroll
-    for (int c = 0; c < 3; ++c) r[REC_DA + c] = da[c];
+    for (int v = 0; v < NG / 4; ++v) {
+        r4[(REC_U >> 2) + v] = make_float4(u[4 * v], u[4 * v + 1], u[4 * v + 2], u[4 * v + 3]);
+        r4[(REC_DL >> 2) + v] = make_float4(dl[4 * v], dl[4 * v + 1], dl[4 * v + 2], dl[4 * v + 3]);
+    }
+    r4[REC_HPRE >> 2] = make_float4(hpre[0], hpre[1], hpre[2], hpre[3]);
+    r4[REC_COEF >> 2] = make_float4(-s * s * vp / static_cast<float>(K), s, 0.f, 0.f);
+    r4[REC_DSIG >> 2] = make_float4(dsig[0], dsig[1], dsig[2], dsig[3]);
+    r4[REC_DA >> 2] = make_float4(da[0], da[1], da[2], 0.f);
 }
 
 // 3. dx += H_pre[i] g_in + phi u + coef x over a K slice, and the partial

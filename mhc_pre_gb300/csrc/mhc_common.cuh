@@ -150,7 +150,9 @@ __device__ __forceinline__ void sinkhorn_fwd(const float* L, int iters, float (&
 // dL = d/dL <dH, Sinkhorn(L)> for the unrolled map (exact reverse mode).
 // The forward keeps each round's row and column sums; walking back, the
 // earlier iterate is rebuilt by multiplying those sums back in, and the VJP
-// of Y = X / s is dX = (dY - sum(dY * Y)) / s along the normalised axis.
+// of Y = X / s is dX = (dY - sum(dY * Y)) / s along the normalised axis
+// (the quotient formed as a product with the correctly rounded 1/s, one
+// reciprocal per row or column instead of four divisions).
 static __device__ __noinline__ void sinkhorn_vjp(const float* L, int iters, const float* dH,
                                           float* dL) {
     float rs[MAX_ITERS][4], cs[MAX_ITERS][4];
@@ -169,9 +171,10 @@ static __device__ __noinline__ void sinkhorn_vjp(const float* L, int iters, cons
         for (int j = 0; j < 4; ++j) {
             const float t = (g[j] * M[j] + g[4 + j] * M[4 + j]) + (g[8 + j] * M[8 + j] + g[12 + j] * M[12 + j]);
             const float c = cs[it][j];
+            const float rc = __frcp_rn(c);   // one reciprocal for the column's four quotients
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                g[4 * i + j] = (g[4 * i + j] - t) / c;
+                g[4 * i + j] = (g[4 * i + j] - t) * rc;
                 M[4 * i + j] *= c;           // rebuild the row-normalised P
             }
         }
@@ -181,9 +184,10 @@ static __device__ __noinline__ void sinkhorn_vjp(const float* L, int iters, cons
             const float t = (g[4 * i] * M[4 * i] + g[4 * i + 1] * M[4 * i + 1]) +
                             (g[4 * i + 2] * M[4 * i + 2] + g[4 * i + 3] * M[4 * i + 3]);
             const float s = rs[it][i];
+            const float rs_i = __frcp_rn(s);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                g[4 * i + j] = (g[4 * i + j] - t) / s;
+                g[4 * i + j] = (g[4 * i + j] - t) * rs_i;
                 M[4 * i + j] *= s;           // rebuild the previous iterate
             }
         }
