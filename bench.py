@@ -16,6 +16,7 @@ arm) on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import collections
 import csv
 import io
 import json
@@ -534,7 +535,12 @@ def run_e2e(args, w, inp, step, stream, dev, world):
     i + 1 are copied on a second stream into a second set of device buffers
     while step i computes; the results of step i are copied back on a third
     stream while step i + 1 computes (the copies, bound by the host link,
-    dominate)."""
+    dominate).  The host keeps at most three steps in flight, as a training
+    loop that reads each step's results does: it waits for the results of
+    step i - 3 to reach the host before it issues step i.  Unbounded, it
+    queues the whole run at once, and every queued step's outputs stay
+    allocated until their copy back ends, which fills the device and makes
+    the allocator free and re-allocate in the middle of the run."""
     import torch
     host = {k: v.to("cpu").pin_memory() for k, v in inp.items()}
     keys = ("x", "y", "g_in", "g_next", "phi", "b", "alpha")
@@ -553,6 +559,8 @@ def run_e2e(args, w, inp, step, stream, dev, world):
     copied = [torch.cuda.Event(), torch.cuda.Event()]
     consumed = [torch.cuda.Event(), torch.cuda.Event()]
     computed = torch.cuda.Event()
+    in_flight = collections.deque()                     # results not yet on the host
+    DEPTH = 3
 
     def copy_in(bi):
         with torch.cuda.stream(copy_stream):
@@ -568,6 +576,9 @@ def run_e2e(args, w, inp, step, stream, dev, world):
             for k, t in res.items():
                 out_h[k].copy_(t, non_blocking=True)
                 t.record_stream(back_stream)            # not reused before the copy is done
+        done = torch.cuda.Event()
+        done.record(back_stream)
+        in_flight.append(done)
 
     def run(n):
         for ev in consumed:
@@ -575,6 +586,8 @@ def run_e2e(args, w, inp, step, stream, dev, world):
         copy_in(0)
         for i in range(n):
             bi = i & 1
+            while len(in_flight) >= DEPTH:
+                in_flight.popleft().synchronize()
             stream.wait_event(copied[bi])
             if i + 1 < n:
                 copy_in(bi ^ 1)
@@ -602,7 +615,8 @@ def run_e2e(args, w, inp, step, stream, dev, world):
             "ms_per_step": ms / steps,
             "path": "pinned host -> device copies (next step's on a second stream, overlapping this "
                     "step's compute), the four C-ABI calls, every result (x_in, x_next, dx, dy, dphi, "
-                    "db, dalpha) -> pinned host on a third stream (overlapping the next step)"}
+                    "db, dalpha) -> pinned host on a third stream (overlapping the next step); at most "
+                    "3 steps in flight (the host waits for step i-3's results before issuing step i)"}
 
 
 def graph_latency_us(fn, dev, calls=20, reps=7):
