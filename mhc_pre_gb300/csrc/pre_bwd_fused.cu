@@ -101,7 +101,7 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t D1_COL = 0;              // one 64-column buffer per stream pair
 constexpr uint32_t D2_COL = 128;            // (chunk, pair) -> 32 columns
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
-constexpr int AHEAD = 2;                    // tiles the first pass may run ahead of the second
+constexpr int LEAD = 15;                    // ring-A positions the first pass may run ahead of ring B
 
 // Rings.  Every consumer of a ring visits each of its positions in order
 // (an mbarrier parity wait is only sound one phase behind):
@@ -111,6 +111,7 @@ constexpr int AHEAD = 2;                    // tiles the first pass may run ahea
 //      p's positions fall in slots p and p + 2 only, so each pair also sees
 //      every phase of its own slots.
 constexpr uint32_t AEMPTY_COUNT = NDOT;
+static_assert(LEAD >= 2 * MAX_NCK, "the first pass must be able to finish the tile ring B waits on");
 constexpr uint32_t BEMPTY_COUNT = 2;
 static_assert(BSLOTS % 2 == 0, "each stream pair owns every other slot of ring B");
 
@@ -291,9 +292,14 @@ pre_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
         // Positions of both rings run over (tile, chunk, stream pair).  Lane 0
         // polls the two rings without blocking; a ring-B box is issued only
         // after the ring-A box of the same position (so that it comes from
-        // L2), and ring A stays at most AHEAD tiles ahead of ring B (so that
-        // the x and g_in it brings in are still in L2 for the second pass:
-        // two tiles of every cluster are about 45 MB).
+        // L2), and ring A stays at most LEAD positions ahead of ring B, so
+        // that the x and g_in it brings in (24 KB a position and CTA, about
+        // 40 MB over 112 CTAs) are still in L2 for the second pass.  At
+        // T = 32768, D = 5120 a lead of 15 positions (a tile and a half) took
+        // 0.900 ms with DRAM reads 1.03x those of a 10-position lead; 10 took
+        // 1.087 ms, 12 0.990, 20-30 0.901-0.910, and up to two whole tiles
+        // ahead 0.906-0.912 with reads 1.08x.  LEAD >= 2 * MAX_NCK, so the
+        // first pass of the tile that ring B waits on can always finish.
         // First pass: normal priority.  An evict-last hint would keep the
         // boxes for the second pass no better (it comes one tile later) and
         // the lines keep that priority after the kernel ends: the next
@@ -306,7 +312,7 @@ pre_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
         while (na < npos || nb < npos) {
             int moved = 0;
             if (lane == 0) {
-                if (na < npos && na / (2 * nck) <= nb / (2 * nck) + AHEAD) {
+                if (na < npos && na - nb <= LEAD) {
                     const int slot = na % ASLOTS;
                     if (ptx::mbar_test_wait(bar(BAR_AEMPTY + slot), ((na / ASLOTS) & 1) ^ 1)) {
                         const int jl = na / (2 * nck), c = (na >> 1) % nck, pr = na & 1;
