@@ -327,11 +327,9 @@ post_norm_bwd_kernel(const TA* __restrict__ g_next, const TA* __restrict__ x, co
 
 // ---- staged backward (bf16 rows that fit in shared memory) ---------------
 // A token's x, g_next and y rows (18 D bytes) arrive in shared memory by
-// bulk copies, so the block-norm pass and the gradient pass read them on chip
-// instead of waiting on global loads in turn.  NBUF = 2: one CTA per SM, the
-// next token's rows copied while this one is worked; NBUF = 1: two CTAs per
-// SM, each copying its next token once done with this one (the other CTA
-// keeps the SM busy meanwhile), with an L2 prefetch one token ahead.  The
+// bulk copies into one of two buffers, the next token's rows while this one
+// is worked (one CTA per SM), so the block-norm pass and the gradient pass
+// read them on chip instead of waiting on global loads in turn.  The
 // per-element expressions are those of the kernel above, evaluated on column
 // pairs with packed fp32 multiply-adds; the sums over the row are formed in
 // another order (per stream and per column parity, then added).  Thread tid
@@ -363,8 +361,8 @@ __device__ __forceinline__ float2 post_elem2(const Gates& g, int i, float2 x0, f
                                  __ffma2_rn(bc2(g.H[i][2]), x2, __ffma2_rn(bc2(g.H[i][1]), x1, __fmul2_rn(bc2(g.H[i][0]), x0)))));
 }
 
-template <int NT, int NBUF, int flags>
-__global__ void __launch_bounds__(NT, 3 - NBUF)
+template <int NT, int flags>
+__global__ void __launch_bounds__(NT, 1)
 post_norm_bwd_staged_kernel(const __nv_bfloat16* __restrict__ g_next, const __nv_bfloat16* __restrict__ x,
                             const __nv_bfloat16* __restrict__ y, const float* __restrict__ H_post,
                             const float* __restrict__ H_res, const float* __restrict__ inv_rms_y,
@@ -373,9 +371,9 @@ post_norm_bwd_staged_kernel(const __nv_bfloat16* __restrict__ g_next, const __nv
                             float* __restrict__ dH_post, float* __restrict__ dH_res) {
     using TA = __nv_bfloat16;
     constexpr int V = 8;
-    extern __shared__ __align__(128) unsigned char stage[];   // NBUF x [x 4D | g 4D | y D]
+    extern __shared__ __align__(128) unsigned char stage[];   // 2 x [x 4D | g 4D | y D]
     __shared__ float red[20 * (NT / 32)];
-    __shared__ __align__(8) uint64_t full[NBUF];
+    __shared__ __align__(8) uint64_t full[2];
     const int tid = threadIdx.x;
     const int64_t QD = D / V;
     const int64_t G = gridDim.x;
@@ -383,7 +381,7 @@ post_norm_bwd_staged_kernel(const __nv_bfloat16* __restrict__ g_next, const __nv
     const uint32_t sb = ptx::smem_u32(stage);
     const uint32_t bar0 = ptx::smem_u32(&full[0]);
     if (tid == 0) {
-        for (int b = 0; b < NBUF; ++b) ptx::mbar_init(bar0 + 8u * b, 1);
+        for (int b = 0; b < 2; ++b) ptx::mbar_init(bar0 + 8u * b, 1);
         ptx::fence_mbar_init();
     }
     __syncthreads();
@@ -396,21 +394,15 @@ post_norm_bwd_staged_kernel(const __nv_bfloat16* __restrict__ g_next, const __nv
         ptx::bulk_load(dst + static_cast<uint32_t>(8 * D), g_next + t * 4 * D, static_cast<uint32_t>(8 * D), bar);
         ptx::bulk_load(dst + static_cast<uint32_t>(16 * D), y + t * D, static_cast<uint32_t>(2 * D), bar);
     };
-    auto prefetch = [&](int64_t t) {
-        bulk_prefetch_l2(x + t * 4 * D, static_cast<uint32_t>(8 * D));
-        bulk_prefetch_l2(g_next + t * 4 * D, static_cast<uint32_t>(8 * D));
-        bulk_prefetch_l2(y + t * D, static_cast<uint32_t>(2 * D));
-    };
     if (tid == 0) {
-        for (int b = 0; b < NBUF; ++b)
+        for (int b = 0; b < 2; ++b)
             if (blockIdx.x + b * G < T) issue(b, blockIdx.x + b * G);
-        if (NBUF == 1 && blockIdx.x + G < T) prefetch(blockIdx.x + G);
     }
     bool aborted = false;
     int k = 0;
     for (int64_t t = blockIdx.x; t < T; t += G, ++k) {
-        const int b = NBUF == 1 ? 0 : (k & 1);
-        const uint32_t par = static_cast<uint32_t>(NBUF == 1 ? k : (k >> 1)) & 1u;
+        const int b = k & 1;
+        const uint32_t par = static_cast<uint32_t>(k >> 1) & 1u;
         const Gates g = load_gates(H_post, H_res, t);
         const float ry = ((flags & SANDWICH) != 0) ? inv_rms_y[t] : 1.0f;
         const float s = ((flags & BLOCK) != 0) ? inv_rms_out[t] : 1.0f;
@@ -434,7 +426,6 @@ post_norm_bwd_staged_kernel(const __nv_bfloat16* __restrict__ g_next, const __nv
             aborted = true;
             break;
         }
-        if (NBUF == 1 && tid == 0 && t + 2 * G < T) prefetch(t + 2 * G);
         TA* xs = reinterpret_cast<TA*>(stage + static_cast<size_t>(b) * buf_bytes);
         TA* gs = xs + 4 * D;
         const TA* ys = xs + 8 * D;
@@ -564,7 +555,7 @@ post_norm_bwd_staged_kernel(const __nv_bfloat16* __restrict__ g_next, const __nv
                 for (int a = 0; a < 20; ++a) red[a * (NT / 32) + wp] = acc[a];
             }
             __syncthreads();   // every thread is done with the buffer
-            if (tid == 0 && t + NBUF * G < T) issue(b, t + NBUF * G);
+            if (tid == 0 && t + 2 * G < T) issue(b, t + 2 * G);
             if (tid < 20) {
                 float tot = 0.f;
 #pragma unroll
@@ -765,12 +756,11 @@ cudaError_t fwd_staged(const void* x, const void* y, const float* H_post, const 
     return cudaGetLastError();
 }
 
-// Buffers per CTA of the staged backward (CTAs per SM: 3 - STG_NBUF) and its
-// width.  At T = 32768, D = 5120 (flags 0 / 1 / 2 / 3): two buffers, 256
-// threads 0.70 / 0.76 / 1.00 / 1.13 ms; one buffer and two CTAs per SM
-// 0.99 / 0.96 / 1.08 / 1.12; two buffers, 320 threads (two pieces each)
-// 0.72 / 0.83 / 1.13 / 1.27; the kernel above 1.24 ms with both flags.
-constexpr int STG_NBUF = 2;
+// Width of the staged backward (two buffers, one CTA per SM).  At T = 32768,
+// D = 5120 (flags 0 / 1 / 2 / 3): 256 threads 0.70 / 0.76 / 1.00 / 1.13 ms;
+// one buffer and two CTAs per SM 0.99 / 0.96 / 1.08 / 1.12; 320 threads (two
+// pieces each) 0.72 / 0.83 / 1.13 / 1.27; the kernel above 1.24 ms with both
+// flags.
 constexpr int STG_NT = 256;
 
 // Shared memory the staged backward may take per CTA on the current device
@@ -784,19 +774,19 @@ size_t staged_smem_limit() {
 }
 
 bool staged_bwd_supports(bool bf16, int64_t D) {
-    return bf16 && D % 8 == 0 && static_cast<size_t>(STG_NBUF * 18 * D) <= staged_smem_limit();
+    return bf16 && D % 8 == 0 && static_cast<size_t>(2 * 18 * D) <= staged_smem_limit();
 }
 
 template <int F>
 cudaError_t bwd_staged(const void* g_next, const void* x, const void* y, const float* H_post, const float* H_res,
                        const float* inv_rms_y, const float* inv_rms_out, int64_t T, int64_t D, void* dx, void* dy,
                        float* dH_post, float* dH_res, cudaStream_t s) {
-    auto k = post_norm_bwd_staged_kernel<STG_NT, STG_NBUF, F>;
-    const size_t smem = static_cast<size_t>(STG_NBUF * 18 * D);
+    auto k = post_norm_bwd_staged_kernel<STG_NT, F>;
+    const size_t smem = static_cast<size_t>(2 * 18 * D);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     using B = __nv_bfloat16;
-    k<<<grid_for(T, 3 - STG_NBUF), STG_NT, smem, s>>>(
+    k<<<grid_for(T, 1), STG_NT, smem, s>>>(
         static_cast<const B*>(g_next), static_cast<const B*>(x), static_cast<const B*>(y), H_post, H_res, inv_rms_y,
         inv_rms_out, T, D, static_cast<B*>(dx), static_cast<B*>(dy), dH_post, dH_res);
     return cudaGetLastError();

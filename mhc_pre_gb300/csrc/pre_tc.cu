@@ -35,7 +35,7 @@
 //     cluster the same way, and only then runs the other gates and Sinkhorn
 //     and writes them out.  Credit barriers (records read, H_pre used) let
 //     consecutive tiles overlap without a cluster-wide rendezvous.
-//   * Nine mix warps form x_in = sum_i H_pre[i] x[i] over the CTA's D-slice:
+//   * Eight mix warps form x_in = sum_i H_pre[i] x[i] over the CTA's D-slice:
 //     x is read from HBM once (TMA, normal L2 priority) and a second time,
 //     soon after, for the mix, from L2.
 //   * Every wait is bounded (about one second); on expiry the kernel latches
