@@ -576,19 +576,29 @@ pre_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
                     if (lane == 0) ptx::mbar_arrive(bar(BAR_D1EMPTY + pp));
                     const unsigned char* gb = box + PBOX + PHIB;
                     // dx increment of this token and stream, written over the
-                    // x row it was computed from (same swizzled place)
+                    // x row it was computed from (same swizzled place); column
+                    // pairs through packed fp32 multiply-adds, each lane rounded
+                    // as fmaf
+                    const float2 hp2 = make_float2(hpre, hpre), cf2 = make_float2(cf, cf);
 #pragma unroll
                     for (int cq = 0; cq < 8; ++cq) {
                         const uint32_t off = static_cast<uint32_t>(t * 128 + ((cq ^ (t & 7)) << 4));
-                        float fx[8], fg[8], o[8];
-                        Vec<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(xb + off), fx);
-                        Vec<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(gb + off), fg);
+                        const uint4 xw = *reinterpret_cast<const uint4*>(xb + off);
+                        const uint4 gw = *reinterpret_cast<const uint4*>(gb + off);
+                        const uint32_t xa[4] = {xw.x, xw.y, xw.z, xw.w}, ga[4] = {gw.x, gw.y, gw.z, gw.w};
+                        uint32_t ow[4];
 #pragma unroll
-                        for (int el = 0; el < 8; ++el) {
-                            const int col = cq * 8 + el;
-                            o[el] = fmaf(hpre, fg[el], fmaf(cf, fx[el], __uint_as_float(v[col >> 4][col & 15])));
+                        for (int w2 = 0; w2 < 4; ++w2) {
+                            const int col = cq * 8 + 2 * w2;
+                            const float2 fx = make_float2(__uint_as_float(xa[w2] << 16), __uint_as_float(xa[w2] & 0xffff0000u));
+                            const float2 fg = make_float2(__uint_as_float(ga[w2] << 16), __uint_as_float(ga[w2] & 0xffff0000u));
+                            const float2 d1 = make_float2(__uint_as_float(v[col >> 4][col & 15]),
+                                                          __uint_as_float(v[(col + 1) >> 4][(col + 1) & 15]));
+                            const float2 o2 = __ffma2_rn(hp2, fg, __ffma2_rn(cf2, fx, d1));
+                            const __nv_bfloat162 ob = __floats2bfloat162_rn(o2.x, o2.y);
+                            ow[w2] = *reinterpret_cast<const uint32_t*>(&ob);
                         }
-                        *reinterpret_cast<uint4*>(xb + off) = Vec<__nv_bfloat16>::pack(o);
+                        *reinterpret_cast<uint4*>(xb + off) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
                     }
                     ptx::fence_proxy_async_smem();
                 }

@@ -172,25 +172,28 @@ __global__ void __launch_bounds__(NT, 1) pre_small_kernel(const Params batch) {
     if (ok) {
         const int RW = KS / NW;                        // a multiple of 8
         const int t = lane / (4 * RP), lg = (lane / RP) & 3, rp = lane % RP;
-        float acc[6] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, sq = 0.f;
-        if (t < T) {
-            const __nv_bfloat16* xr = reinterpret_cast<const __nv_bfloat16*>(smem + L.xs + t * L.xrow);
-            for (int k0 = warp * RW; k0 < (warp + 1) * RW; k0 += 8) {
+        float acc[6], sq = 0.f;
+        {
+            // logit pairs through packed fp32 multiply-adds (each lane rounds
+            // as fmaf: the same chain per logit as one at a time)
+            float2 a01 = make_float2(0.f, 0.f), a23 = a01, a45 = a01;
+            if (t < T) {
+                const __nv_bfloat16* xr = reinterpret_cast<const __nv_bfloat16*>(smem + L.xs + t * L.xrow);
+                for (int k0 = warp * RW; k0 < (warp + 1) * RW; k0 += 8) {
 #pragma unroll
-                for (int i = 0; i < 8 / RP; ++i) {
-                    const int k = k0 + rp + RP * i;
-                    const float xv = __bfloat162float(xr[k]);
-                    const float2* ph2 = reinterpret_cast<const float2*>(phs + k * NG + 6 * lg);
-                    const float2 p0 = ph2[0], p1 = ph2[1], p2 = ph2[2];
-                    acc[0] = fmaf(xv, p0.x, acc[0]);
-                    acc[1] = fmaf(xv, p0.y, acc[1]);
-                    acc[2] = fmaf(xv, p1.x, acc[2]);
-                    acc[3] = fmaf(xv, p1.y, acc[3]);
-                    acc[4] = fmaf(xv, p2.x, acc[4]);
-                    acc[5] = fmaf(xv, p2.y, acc[5]);
-                    if (lg == 0) sq = fmaf(xv, xv, sq);
+                    for (int i = 0; i < 8 / RP; ++i) {
+                        const int k = k0 + rp + RP * i;
+                        const float xv = __bfloat162float(xr[k]);
+                        const float2 xv2 = make_float2(xv, xv);
+                        const float2* ph2 = reinterpret_cast<const float2*>(phs + k * NG + 6 * lg);
+                        a01 = __ffma2_rn(xv2, ph2[0], a01);
+                        a23 = __ffma2_rn(xv2, ph2[1], a23);
+                        a45 = __ffma2_rn(xv2, ph2[2], a45);
+                        if (lg == 0) sq = fmaf(xv, xv, sq);
+                    }
                 }
             }
+            acc[0] = a01.x; acc[1] = a01.y; acc[2] = a23.x; acc[3] = a23.y; acc[4] = a45.x; acc[5] = a45.y;
         }
 #pragma unroll
         for (int m = 1; m < RP; m <<= 1) {
