@@ -46,6 +46,30 @@ template <> struct Vec<__nv_bfloat16> {
     }
 };
 
+// x_in of one 16-byte piece (8 columns): sum_i h[i] x_i for the four
+// streams' pieces, h.x x_0 first, then one fmaf per stream, rounded to bf16
+// once.  Column pairs go through packed fp32 multiply-adds; each lane rounds
+// as the scalar product and fmaf chain would.
+__device__ __forceinline__ uint4 mix4_bf16(const uint4& x0, const uint4& x1, const uint4& x2, const uint4& x3,
+                                           const float4& h) {
+    const float2 hx = make_float2(h.x, h.x), hy = make_float2(h.y, h.y);
+    const float2 hz = make_float2(h.z, h.z), hw = make_float2(h.w, h.w);
+    const uint32_t a0[4] = {x0.x, x0.y, x0.z, x0.w}, a1[4] = {x1.x, x1.y, x1.z, x1.w};
+    const uint32_t a2[4] = {x2.x, x2.y, x2.z, x2.w}, a3[4] = {x3.x, x3.y, x3.z, x3.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 f0 = make_float2(__uint_as_float(a0[q] << 16), __uint_as_float(a0[q] & 0xffff0000u));
+        const float2 f1 = make_float2(__uint_as_float(a1[q] << 16), __uint_as_float(a1[q] & 0xffff0000u));
+        const float2 f2 = make_float2(__uint_as_float(a2[q] << 16), __uint_as_float(a2[q] & 0xffff0000u));
+        const float2 f3 = make_float2(__uint_as_float(a3[q] << 16), __uint_as_float(a3[q] & 0xffff0000u));
+        const float2 v = __ffma2_rn(hw, f3, __ffma2_rn(hz, f2, __ffma2_rn(hy, f1, __fmul2_rn(hx, f0))));
+        const __nv_bfloat162 b = __floats2bfloat162_rn(v.x, v.y);
+        o[q] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 template <> struct Vec<float> {
     static constexpr int N = 4;
     __device__ __forceinline__ static void unpack(const uint4& u, float (&f)[4]) {

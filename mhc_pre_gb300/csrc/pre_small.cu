@@ -265,14 +265,7 @@ __global__ void __launch_bounds__(NT, 1) pre_small_kernel(const Params batch) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) xv[i] = ld16(src + static_cast<int64_t>(i) * D);
             const float4 h = hb[t];
-            float f0[8], f1[8], f2[8], f3[8], o[8];
-            Vec<__nv_bfloat16>::unpack(xv[0], f0);
-            Vec<__nv_bfloat16>::unpack(xv[1], f1);
-            Vec<__nv_bfloat16>::unpack(xv[2], f2);
-            Vec<__nv_bfloat16>::unpack(xv[3], f3);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o[e] = fmaf(h.w, f3[e], fmaf(h.z, f2[e], fmaf(h.y, f1[e], h.x * f0[e])));
-            st16_stream(p.x_in + static_cast<int64_t>(t) * D + qq * 8, Vec<__nv_bfloat16>::pack(o));
+            st16_stream(p.x_in + static_cast<int64_t>(t) * D + qq * 8, mix4_bf16(xv[0], xv[1], xv[2], xv[3], h));
         }
     }
     // ---- the owner: the other gates (off the mix's path) -------------------

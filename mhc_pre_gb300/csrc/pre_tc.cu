@@ -633,17 +633,8 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
 #pragma unroll
                 for (int m = 0; m < MIX_UNROLL; ++m) {
                     if (tok[m] < p.T) {
-                        const float4 h = hb[rr[m]];
-                        float f0[8], f1[8], f2[8], f3[8], o[8];
-                        Vec<__nv_bfloat16>::unpack(xv[m][0], f0);
-                        Vec<__nv_bfloat16>::unpack(xv[m][1], f1);
-                        Vec<__nv_bfloat16>::unpack(xv[m][2], f2);
-                        Vec<__nv_bfloat16>::unpack(xv[m][3], f3);
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            o[q] = fmaf(h.w, f3[q], fmaf(h.z, f2[q], fmaf(h.y, f1[q], h.x * f0[q])));
                         st16_stream(p.x_in + tok[m] * D + static_cast<int64_t>(c) * Dc + qq[m] * 8,
-                                    Vec<__nv_bfloat16>::pack(o));
+                                    mix4_bf16(xv[m][0], xv[m][1], xv[m][2], xv[m][3], hb[rr[m]]));
                     }
                 }
             }
