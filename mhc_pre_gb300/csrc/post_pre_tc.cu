@@ -653,14 +653,23 @@ post_pre_mix_kernel(const __nv_bfloat16* __restrict__ x_next, const float* H_pre
         if (tid < nt) hp[tid] = __ldcg(reinterpret_cast<const float4*>(H_pre) + t0 + tid);
         __syncthreads();
         const int items = nt * qpt;
+        // item idx = (row r, piece q), idx = r qpt + q; a thread's item moves by
+        // MIX_THREADS a step, so r and q advance with a carry (no division)
+        const int dr = MIX_THREADS / qpt, dq = MIX_THREADS - dr * qpt;
+        int r_at = tid / qpt, q_at = tid - r_at * qpt;
         for (int base = 0; base < items; base += MIX_THREADS * MIX_UNROLL) {
             uint4 xv[MIX_UNROLL][4];
             int rr[MIX_UNROLL], qq[MIX_UNROLL];
 #pragma unroll
             for (int m = 0; m < MIX_UNROLL; ++m) {
-                const int idx = base + m * MIX_THREADS + tid;
-                rr[m] = idx < items ? idx / qpt : -1;
-                qq[m] = idx - (idx / qpt) * qpt;
+                rr[m] = r_at < nt ? r_at : -1;
+                qq[m] = q_at;
+                q_at += dq;
+                r_at += dr;
+                if (q_at >= qpt) {
+                    q_at -= qpt;
+                    ++r_at;
+                }
                 if (rr[m] >= 0) {
                     const uint4* src = reinterpret_cast<const uint4*>(x_next + (t0 + rr[m]) * K + qq[m] * 8);
 #pragma unroll

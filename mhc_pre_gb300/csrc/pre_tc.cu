@@ -614,16 +614,26 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
             const int qpt = Dc / 8;
             // no x_in buffer: the gates alone (recompute of the saved state)
             const int items = (ok && p.x_in != nullptr) ? TILE_M * qpt : 0;
+            // item idx = (row r, piece q) with idx = r qpt + q; each step moves a
+            // thread's item by NMIX * 32, so r and q advance by a fixed amount
+            // with a carry instead of a division per item
+            const int dr = (NMIX * 32) / qpt, dq = (NMIX * 32) - dr * qpt;
+            int r_at = mtid / qpt, q_at = mtid - r_at * qpt;
             for (int base = 0; base < items; base += NMIX * 32 * MIX_UNROLL) {
                 uint4 xv[MIX_UNROLL][4];
                 int64_t tok[MIX_UNROLL];
                 int qq[MIX_UNROLL], rr[MIX_UNROLL];
 #pragma unroll
                 for (int m = 0; m < MIX_UNROLL; ++m) {
-                    const int idx = base + m * NMIX * 32 + mtid;
-                    rr[m] = idx / qpt;
-                    qq[m] = idx - rr[m] * qpt;
-                    tok[m] = (idx < items) ? t0 + rr[m] : p.T;
+                    rr[m] = r_at;
+                    qq[m] = q_at;
+                    tok[m] = (r_at < TILE_M) ? t0 + r_at : p.T;
+                    q_at += dq;
+                    r_at += dr;
+                    if (q_at >= qpt) {
+                        q_at -= qpt;
+                        ++r_at;
+                    }
                     if (tok[m] < p.T) {
                         const __nv_bfloat16* src = p.x + tok[m] * K + static_cast<int64_t>(c) * Dc + qq[m] * 8;
 #pragma unroll
