@@ -654,34 +654,42 @@ post_pre_mix_kernel(const __nv_bfloat16* __restrict__ x_next, const float* H_pre
         __syncthreads();
         const int items = nt * qpt;
         // item idx = (row r, piece q), idx = r qpt + q; a thread's item moves by
-        // MIX_THREADS a step, so r and q advance with a carry (no division)
+        // MIX_THREADS a step, so r, q and the item's offsets into x_next and
+        // x_in advance with a carry (no division or multiply per item)
         const int dr = MIX_THREADS / qpt, dq = MIX_THREADS - dr * qpt;
         int r_at = tid / qpt, q_at = tid - r_at * qpt;
+        int64_t xo_at = (t0 + r_at) * K + q_at * 8, io_at = (t0 + r_at) * D + q_at * 8;
+        const int64_t xstep = dr * K + dq * 8, xcarry = K - qpt * 8;
+        const int64_t istep = static_cast<int64_t>(dr) * D + dq * 8, icarry = static_cast<int64_t>(D) - qpt * 8;
         for (int base = 0; base < items; base += MIX_THREADS * MIX_UNROLL) {
             uint4 xv[MIX_UNROLL][4];
-            int rr[MIX_UNROLL], qq[MIX_UNROLL];
+            int64_t io[MIX_UNROLL];
+            int rr[MIX_UNROLL];
 #pragma unroll
             for (int m = 0; m < MIX_UNROLL; ++m) {
                 rr[m] = r_at < nt ? r_at : -1;
-                qq[m] = q_at;
+                io[m] = io_at;
+                const int64_t xo = xo_at;
                 q_at += dq;
                 r_at += dr;
+                xo_at += xstep;
+                io_at += istep;
                 if (q_at >= qpt) {
                     q_at -= qpt;
                     ++r_at;
+                    xo_at += xcarry;
+                    io_at += icarry;
                 }
                 if (rr[m] >= 0) {
-                    const uint4* src = reinterpret_cast<const uint4*>(x_next + (t0 + rr[m]) * K + qq[m] * 8);
+                    const uint4* src = reinterpret_cast<const uint4*>(x_next + xo);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) xv[m][i] = __ldcg(src + static_cast<int64_t>(i) * (D / 8));
                 }
             }
 #pragma unroll
             for (int m = 0; m < MIX_UNROLL; ++m) {
-                if (rr[m] >= 0) {
-                    st16_stream(x_in + (t0 + rr[m]) * D + qq[m] * 8,
-                                mix4_bf16(xv[m][0], xv[m][1], xv[m][2], xv[m][3], hp[rr[m]]));
-                }
+                if (rr[m] >= 0)
+                    st16_stream(x_in + io[m], mix4_bf16(xv[m][0], xv[m][1], xv[m][2], xv[m][3], hp[rr[m]]));
             }
         }
         __syncthreads();   // hp is refilled for the next tile

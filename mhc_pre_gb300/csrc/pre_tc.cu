@@ -615,37 +615,45 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
             // no x_in buffer: the gates alone (recompute of the saved state)
             const int items = (ok && p.x_in != nullptr) ? TILE_M * qpt : 0;
             // item idx = (row r, piece q) with idx = r qpt + q; each step moves a
-            // thread's item by NMIX * 32, so r and q advance by a fixed amount
-            // with a carry instead of a division per item
+            // thread's item by NMIX * 32, so r, q and the item's offsets into x
+            // and x_in advance by fixed amounts with a carry (no division or
+            // multiply per item)
             const int dr = (NMIX * 32) / qpt, dq = (NMIX * 32) - dr * qpt;
+            const int rlim = p.T - t0 < TILE_M ? static_cast<int>(p.T - t0) : TILE_M;   // rows in the batch
             int r_at = mtid / qpt, q_at = mtid - r_at * qpt;
+            int64_t xo_at = (t0 + r_at) * K + static_cast<int64_t>(c) * Dc + q_at * 8;
+            int64_t io_at = (t0 + r_at) * D + static_cast<int64_t>(c) * Dc + q_at * 8;
+            const int64_t xstep = dr * K + dq * 8, xcarry = K - qpt * 8;
+            const int64_t istep = static_cast<int64_t>(dr) * D + dq * 8, icarry = D - qpt * 8;
             for (int base = 0; base < items; base += NMIX * 32 * MIX_UNROLL) {
                 uint4 xv[MIX_UNROLL][4];
-                int64_t tok[MIX_UNROLL];
-                int qq[MIX_UNROLL], rr[MIX_UNROLL];
+                int64_t io[MIX_UNROLL];
+                int rr[MIX_UNROLL];
 #pragma unroll
                 for (int m = 0; m < MIX_UNROLL; ++m) {
-                    rr[m] = r_at;
-                    qq[m] = q_at;
-                    tok[m] = (r_at < TILE_M) ? t0 + r_at : p.T;
+                    rr[m] = r_at < rlim ? r_at : -1;
+                    io[m] = io_at;
+                    const int64_t xo = xo_at;
                     q_at += dq;
                     r_at += dr;
+                    xo_at += xstep;
+                    io_at += istep;
                     if (q_at >= qpt) {
                         q_at -= qpt;
                         ++r_at;
+                        xo_at += xcarry;
+                        io_at += icarry;
                     }
-                    if (tok[m] < p.T) {
-                        const __nv_bfloat16* src = p.x + tok[m] * K + static_cast<int64_t>(c) * Dc + qq[m] * 8;
+                    if (rr[m] >= 0) {
+                        const __nv_bfloat16* src = p.x + xo;
 #pragma unroll
                         for (int i = 0; i < 4; ++i) xv[m][i] = ld16_stream(src + static_cast<int64_t>(i) * D);
                     }
                 }
 #pragma unroll
                 for (int m = 0; m < MIX_UNROLL; ++m) {
-                    if (tok[m] < p.T) {
-                        st16_stream(p.x_in + tok[m] * D + static_cast<int64_t>(c) * Dc + qq[m] * 8,
-                                    mix4_bf16(xv[m][0], xv[m][1], xv[m][2], xv[m][3], hb[rr[m]]));
-                    }
+                    if (rr[m] >= 0)
+                        st16_stream(p.x_in + io[m], mix4_bf16(xv[m][0], xv[m][1], xv[m][2], xv[m][3], hb[rr[m]]));
                 }
             }
             // every mix thread is done with this tile's H_pre buffer: arm it
