@@ -8,7 +8,6 @@ parameter gradients; with fake addresses those calls are only checked for
 their refusals here, and tests/test_gpu_parity.py checks the zeros on a GPU.)
 """
 
-import ctypes
 import os
 import re
 

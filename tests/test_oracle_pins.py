@@ -11,7 +11,6 @@ eps) breaks at least one of them.
 import math
 
 import numpy as np
-import pytest
 import scipy.special
 
 from oracle import mhc_oracle as O
